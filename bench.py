@@ -1,0 +1,427 @@
+"""Benchmark: decode-attention tokens/s and achieved HBM GB/s on one GB300.
+
+A step is one pass of the whole hot path over one batch: kv_append of the new
+K/V row of every (sequence, kv head), then decode_attn over the cache.  The
+step cycles through 16 consecutive positions (context n+1 ... n+16, as in
+the MHA fp32 workload's 16 append+decode steps), so the context length is the
+same however many steps run.  Inputs are seeded synthetic tensors resident in
+HBM before timing; K/V copies are rotated so that the cache bytes touched
+between two reads of the same copy exceed 4x the L2 size.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead.  Under torchrun every rank runs an independent
+replica (its own batch; no collective on the data path); timing is the max
+over ranks and ``value`` counts all ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decode_attention_kv_split_gb300 import accounting, workloads as W  # noqa: E402
+
+METRIC = "decode-attn tokens/s and achieved HBM GB/s (% of GB300 peak) vs context"
+L2_BYTES = 129 * 1024 * 1024
+CYCLE = 16
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_kv_split_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu capture, if it was taken
+    on the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inwin = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e30)]
+        use = inwin if inwin else rows
+        sm = sorted(r[1] for r in use)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if "Active" in v
+                          and "Not" not in v})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inwin)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(w, n_rot: int, kv_bytes: int):
+    cfg = {"workload": w.description, "name": w.name, "B": w.B, "h_q": w.h_q, "h_kv": w.h_kv,
+           "d_k": w.d_k, "d_v": w.d_v, "n_start": w.n, "context": f"n+1 .. n+{CYCLE}",
+           "n_max_allocated": w.n_max + CYCLE, "kv_dtype": str(w.dtype).replace("torch.", ""),
+           "num_splits": w.num_splits or "auto", "parallelism": "replicas (one per GPU)",
+           "tokens_per_step": w.B}
+    if w.ragged:
+        cfg["lengths"] = f"uniform in [{w.ragged[0]}, {w.ragged[1]}] (seed 3)"
+    if n_rot * kv_bytes >= 4 * L2_BYTES:
+        cfg["l2"] = (f"{n_rot} rotating K/V copies of {kv_bytes / 1e6:.0f} MB each "
+                     f"(>= 4x the {L2_BYTES >> 20} MiB L2 between reuses)")
+    else:
+        cfg["l2"] = (f"L2-resident: {n_rot} K/V copies of {kv_bytes / 1e6:.2f} MB; "
+                     "latency only, GB/s not meaningful")
+    return cfg
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_step_sample(w, budget_s: float, threads: int):
+    """Time the oracle's decode on a bounded sample of the workload's (b, h)
+    heads at context n+1.  Returns (tokens/s equivalent, sample text, cores)."""
+    import numpy as np
+    import oracle
+
+    o = oracle.get()
+    cores = min(threads, o.max_threads())
+    lens = W.seq_lens(w)
+    q = W.query(w).float().numpy()
+    # one kv head's rows are shared by its group; sample whole groups of heads
+    n1 = int(lens[0]) + 1
+    g = np.random.default_rng(0)
+    Kh = g.standard_normal((n1, w.d_k)).astype(np.float32)
+    Vh = g.standard_normal((n1, w.d_v)).astype(np.float32)
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        o.decode_head(q[0, heads % w.h_q], Kh, Vh, w.scale)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    # every token needs B*h_q heads at this context length (ragged: mean length)
+    mean_len = float(lens.double().mean()) + 1
+    heads_per_token = w.h_q * (mean_len / n1)
+    tok_s = heads / heads_per_token / el
+    return tok_s, (f"oracle decode_head (fp64, 1 thread) on {heads} single heads at n={n1} "
+                   f"for {el:.1f} s, scaled to B*h_q heads per token at mean context "
+                   f"{mean_len:.0f}"), 1
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_step_sample(w, budget / 4, 1)
+    t0 = time.perf_counter()
+    vals = []
+    sample = ""
+    for _ in range(args.steps):
+        v, sample, cores = oracle_step_sample(w, budget, 1)
+        vals.append(v)
+    el = time.perf_counter() - t0
+    value = sum(vals) / len(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, 1, 0),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, w, world, rank, local):
+    from decode_attention_kv_split_gb300 import api
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    torch.manual_seed(rank)
+    n_max = w.n_max + CYCLE
+    wb = W.custom(name=w.name, B=w.B, h_q=w.h_q, h_kv=w.h_kv, d_k=w.d_k, d_v=w.d_v, n=w.n,
+                  n_max=n_max, dtype=w.dtype, kv_std=w.kv_std, ragged=w.ragged,
+                  num_splits=w.num_splits, description=w.description)
+    seed = 1000 * rank
+    lens0 = W.seq_lens(wb, seed)
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    kv_touch = accounting.decode_bytes((lens0 + CYCLE).tolist(), w.h_q, w.h_kv, w.d_k, w.d_v, es)
+    n_rot = max(1, math.ceil(4 * L2_BYTES / kv_touch))
+    cache_bytes = 2 * wb.B * wb.h_kv * n_max * wb.d_k * es
+    free = torch.cuda.mem_get_info(dev)[0]
+    n_rot = int(max(1, min(n_rot, 64, (0.6 * free) // cache_bytes)))
+
+    K0, V0 = W.cache(wb, seed)
+    caches = []
+    for r in range(n_rot):
+        caches.append((K0.to(dev), V0.to(dev)))
+    del K0, V0
+    q = W.query(wb, seed).to(dev)
+    rows = [W.new_rows(wb, t, seed) for t in range(CYCLE)]
+    k_new = [k.to(dev) for k, _ in rows]
+    v_new = [v.to(dev) for _, v in rows]
+    pos_t = [(lens0 + t).to(torch.int32).to(dev) for t in range(CYCLE)]
+    lens_t = [(lens0 + t + 1).to(torch.int32).to(dev) for t in range(CYCLE)]
+    out = torch.empty((wb.B, wb.h_q, wb.d_v), dtype=torch.float32, device=dev)
+    splits = api.resolve_splits(wb.B, wb.h_q, wb.h_kv, wb.d_k, wb.d_v, n_max, wb.dtype, w.num_splits)
+    ws_bytes = api.workspace_bytes(wb.B, wb.h_q, wb.h_kv, wb.d_k, wb.d_v, n_max, wb.dtype, w.num_splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        K, V = caches[i % n_rot]
+        c = i % CYCLE
+        api.kv_append(k_new[c], v_new[c], K, V, pos_t[c])
+        api.decode_attn(q, K, V, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    if sampler:
+        sampler.mark(True)
+    ev_start.record(stream)
+    for i in range(K):
+        Kc, Vc = caches[i % n_rot]
+        c = i % CYCLE
+        ev[i][0].record(stream)
+        api.kv_append(k_new[c], v_new[c], Kc, Vc, pos_t[c])
+        ev[i][1].record(stream)
+        api.decode_attn(q, Kc, Vc, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+        ev[i][2].record(stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
+    barrier(world)
+    launches = api.launch_count() - launches0
+    total_ms = ev_start.elapsed_time(ev_end)
+    total_ms = max_over_ranks(total_ms, world)
+    append_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    clocks = sampler.stop() if sampler else None
+
+    # ---- end to end: pinned host inputs in, result out, every step
+    q_h = q.cpu().pin_memory()
+    kn_h = [k.cpu().pin_memory() for k in k_new]
+    vn_h = [v.cpu().pin_memory() for v in v_new]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d = torch.empty_like(q)
+    kn_d = torch.empty_like(k_new[0])
+    vn_d = torch.empty_like(v_new[0])
+    e2e_steps = max(1, min(K, 2000))
+    for i in range(min(args.warmup, 8)):
+        c = i % CYCLE
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h[c], non_blocking=True)
+        vn_d.copy_(vn_h[c], non_blocking=True)
+        Kc, Vc = caches[i % n_rot]
+        api.kv_append(kn_d, vn_d, Kc, Vc, pos_t[c])
+        api.decode_attn(q_d, Kc, Vc, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        c = i % CYCLE
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h[c], non_blocking=True)
+        vn_d.copy_(vn_h[c], non_blocking=True)
+        Kc, Vc = caches[i % n_rot]
+        api.kv_append(kn_d, vn_d, Kc, Vc, pos_t[c])
+        api.decode_attn(q_d, Kc, Vc, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = q.numel() * q.element_size() + 2 * k_new[0].numel() * k_new[0].element_size()
+    d2h = out.numel() * out.element_size()
+
+    if rank != 0:
+        return
+    # ---- accounting
+    mean_lens = [int(n) + (CYCLE + 1) / 2 for n in lens0.tolist()]
+    dec_bytes = accounting.decode_bytes(mean_lens, w.h_q, w.h_kv, w.d_k, w.d_v, es)
+    app_bytes = accounting.append_bytes(w.B, w.h_kv, w.d_k, w.d_v, es)
+    ms_per_step = total_ms / K
+    tokens_per_s = world * w.B / (ms_per_step / 1e3)
+    peak, peak_kind = peaks()
+    achieved = dec_bytes / (decode_ms / 1e3) / 1e9
+    traffic = recorded_traffic(w.name)
+    bytes_str = f"{dec_bytes / 1e6:.1f} MB per decode launch"
+    if w.B * w.h_kv * w.n * (w.d_k + w.d_v) * es < L2_BYTES:
+        bytes_str += " (L2-resident)"
+
+    cpu_v, cpu_sample, cpu_cores = oracle_step_sample(wb, args.cpu_seconds, 1)
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.dtype == torch.float32 else "bf16",
+        "data": "synthetic", "config": workload_config(wb, n_rot, kv_touch),
+        "hbm_gbs": (dec_bytes + app_bytes) / (ms_per_step / 1e3) / 1e9,
+        "hbm_frac_of_8tbs": (dec_bytes + app_bytes) / (ms_per_step / 1e3) / 8e12,
+        "decode_ms": decode_ms, "append_ms": append_ms, "num_splits": splits,
+        "roofline": {"bound": "hbm", "kernel": "decode_attn (split kernel"
+                     + (" + LSE combine)" if splits > 1 else ")"),
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": traffic, "algorithmic_bytes": dec_bytes, "per": bytes_str},
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
+                         "sample": cpu_sample},
+        "e2e": {"value": world * w.B * e2e_steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "sync": "host waits for each step's result"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mha_fp32", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -6,3 +6,12 @@ this package is the thin Python binding over it.  Importing the package does
 not load the library; the first call does, and raises if it is missing.
 """
 from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
+from .api import (  # noqa: F401
+    DecodeAttnError,
+    decode_attn,
+    decode_attn_owned,
+    kv_append,
+    launch_count,
+    resolve_splits,
+    workspace_bytes,
+)

@@ -1,0 +1,209 @@
+"""Python binding over libdecode_attn.so (ctypes; argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels.  This
+module checks tensor shapes/dtypes/devices, takes raw device pointers and the
+current CUDA stream from PyTorch, allocates the split workspace with PyTorch,
+and calls the C entry points of the same names.  There is no CPU fallback:
+if the shared library is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdecode_attn.so")
+
+DA_FP32 = 0
+DA_BF16 = 1
+DEVERR_SEQ_LEN = 1
+DEVERR_POS = 2
+DEVERR_TIMEOUT = 4
+
+_DTYPES = {torch.float32: DA_FP32, torch.bfloat16: DA_BF16}
+
+_lock = threading.Lock()
+_lib = None
+
+# Every entry point of include/decode_attn.h with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "decode_attn_resolve_splits": (_I, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "decode_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
+    "decode_attn_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
+    "decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "decode_attn_status_string": (ctypes.c_char_p, [_I]),
+    "decode_attn_last_cuda_error": (ctypes.c_char_p, []),
+    "decode_attn_launch_count": (ctypes.c_uint64, []),
+}
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load()
+        msg = lib.decode_attn_status_string(status).decode()
+        if status == -6:
+            msg += ": " + lib.decode_attn_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library once; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with __graft_entry__.build() "
+                    "(there is no fallback implementation)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise DecodeAttnError(status, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cache_dims(q, K, V, seq_lens):
+    if q.dim() != 3 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("expected q [B, h_q, d_k], K [B, h_kv, n_max, d_k], V [B, h_kv, n_max, d_v]")
+    B, h_q, d_k = q.shape
+    Bk, h_kv, n_max, d_k2 = K.shape
+    Bv, h_kv2, n_max2, d_v = V.shape
+    if (Bk, Bv) != (B, B) or h_kv2 != h_kv or n_max2 != n_max or d_k2 != d_k:
+        raise ValueError("q, K and V shapes disagree")
+    if seq_lens.shape != (B,) or seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be an int32 tensor of shape [B]")
+    for name, t in (("q", q), ("K", K), ("V", V), ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if not (q.dtype == K.dtype == V.dtype) or q.dtype not in _DTYPES:
+        raise ValueError("q, K, V must share dtype float32 or bfloat16")
+    return B, h_q, h_kv, d_k, d_v, n_max
+
+
+def resolve_splits(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_splits: int = 0) -> int:
+    """Splits per (b, kv head) the library uses for this request (on the current device)."""
+    r = load().decode_attn_resolve_splits(B, h_q, h_kv, d_k, d_v, n_max, _DTYPES[dtype], num_splits)
+    if r < 0:
+        raise DecodeAttnError(r, "decode_attn_resolve_splits")
+    return r
+
+
+def workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_splits: int = 0) -> int:
+    st = ctypes.c_int(0)
+    n = load().decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, _DTYPES[dtype], num_splits,
+                                           ctypes.byref(st))
+    _check(st.value, "decode_attn_workspace_bytes")
+    return int(n)
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def decode_attn(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, seq_lens: torch.Tensor,
+                out: torch.Tensor | None = None, scale: float | None = None, num_splits: int = 0,
+                workspace: torch.Tensor | None = None, dev_error: torch.Tensor | None = None,
+                stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Decode attention (calls ``decode_attn_ex``); returns ``out`` [B, h_q, d_v] float32.
+
+    ``scale`` defaults to 1/sqrt(d_k).  ``workspace`` (uint8 CUDA tensor) is
+    allocated and cached per stream when not given.  ``dev_error`` is an
+    optional int32 CUDA scalar the kernels OR error bits into.
+    """
+    B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    if out is None:
+        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
+    elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
+    dt = _DTYPES[q.dtype]
+    lib = load()
+    with torch.cuda.device(q.device):
+        need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, q.dtype, num_splits)
+        if workspace is None:
+            workspace = _workspace(q.device, need)
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.decode_attn_ex(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q, h_kv,
+                                d_k, d_v, n_max, float(scale), dt, int(num_splits), _ptr(workspace),
+                                nbytes, _ptr(dev_error), _stream(q, stream))
+    _check(st, "decode_attn_ex")
+    return out
+
+
+def decode_attn_owned(q, K, V, seq_lens, out=None, scale=None, stream=None) -> torch.Tensor:
+    """Decode attention through ``decode_attn`` (library-owned workspace)."""
+    B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    if out is None:
+        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = load().decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q, h_kv,
+                                d_k, d_v, n_max, float(scale), _DTYPES[q.dtype], _stream(q, stream))
+    _check(st, "decode_attn")
+    return out
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+              pos: torch.Tensor, dev_error: torch.Tensor | None = None,
+              stream: torch.cuda.Stream | None = None) -> None:
+    """Write row pos[b] of every (b, kv head) of K and V in place (exact copy)."""
+    if K.dim() != 4 or V.dim() != 4:
+        raise ValueError("K, V must be [B, h_kv, n_max, d]")
+    B, h_kv, n_max, d_k = K.shape
+    d_v = V.shape[3]
+    if k_new.shape != (B, h_kv, d_k) or v_new.shape != (B, h_kv, d_v) or V.shape[:3] != K.shape[:3]:
+        raise ValueError("k_new/v_new/K/V shapes disagree")
+    if pos.shape != (B,) or pos.dtype != torch.int32:
+        raise ValueError("pos must be an int32 tensor of shape [B]")
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("K", K), ("V", V), ("pos", pos)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if not (k_new.dtype == v_new.dtype == K.dtype == V.dtype) or K.dtype not in _DTYPES:
+        raise ValueError("k_new, v_new, K, V must share dtype float32 or bfloat16")
+    with torch.cuda.device(K.device):
+        st = load().kv_append(_ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V), _ptr(pos), B, h_kv, d_k,
+                              d_v, n_max, _DTYPES[K.dtype], _ptr(dev_error), _stream(K, stream))
+    _check(st, "kv_append")
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(load().decode_attn_launch_count())

@@ -1,0 +1,361 @@
+// Host side of the C ABI declared in include/decode_attn.h: argument checks,
+// split planning, TMA descriptor encoding, workspace handling and launches.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+using da::KernelShape;
+using da::SplitParams;
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_last_cuda_error[256] = "";
+
+int fail_cuda(cudaError_t e, const char* what) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%d)", what,
+           cudaGetErrorString(e), int(e));
+  return DA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Device properties, cached per device ordinal.
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+  int checked = 0;
+  int ok = 0;
+  int sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int current_device(int* dev, int* sms) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return DA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[*dev];
+  if (!di.checked) {
+    int major = 0, minor = 0, count = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess)
+      return fail_cuda(e, "cudaDeviceGetAttribute");
+    di.ok = (major == 10 && minor == 3);
+    di.sms = count;
+    di.checked = 1;
+  }
+  *sms = di.sms;
+  return di.ok ? DA_OK : DA_ERR_DEVICE;
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-map encoding through the driver entry point (no libcuda link).
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+int get_encoder(EncodeTiledFn* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                    cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!g_encode) return fail_cuda(g_encode_err == cudaSuccess ? cudaErrorNotSupported : g_encode_err,
+                                  "cuTensorMapEncodeTiled entry point");
+  *fn = g_encode;
+  return DA_OK;
+}
+
+// A [rows_total = B*h_kv heads][n_max][d] cache viewed as a 3-D tensor
+// (innermost first): x = column, y = row inside a head, z = b*h_kv + head.
+int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int d, int n_max, int heads,
+                     const KernelShape& ks) {
+  EncodeTiledFn fn;
+  int st = get_encoder(&fn);
+  if (st != DA_OK) return st;
+  const int es = dtype == DA_BF16 ? 2 : 4;
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(n_max), cuuint64_t(heads)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * es, cuuint64_t(n_max) * d * es};
+  const cuuint32_t box[3] = {cuuint32_t(ks.box_cols), cuuint32_t(ks.tile_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype == DA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  ks.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
+             int(r));
+    return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Argument checks and split planning.
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype) {
+  if (dtype != DA_FP32 && dtype != DA_BF16) return DA_ERR_DTYPE;
+  if (B <= 0 || h_q <= 0 || h_kv <= 0 || n_max <= 0) return DA_ERR_SHAPE;
+  if (h_q % h_kv != 0) return DA_ERR_SHAPE;
+  if (n_max > (1 << 30)) return DA_ERR_SHAPE;
+  if ((long long)B * h_kv * (long long)n_max > 0x7fffffffLL) return DA_ERR_SHAPE;
+  if ((long long)B * h_q > 0x7fffffffLL) return DA_ERR_SHAPE;
+  if (d_k != d_v) return DA_ERR_UNSUPPORTED;
+  if (d_k != 64 && d_k != 128) return DA_ERR_UNSUPPORTED;
+  return DA_OK;
+}
+
+struct Plan {
+  KernelShape ks;
+  int head_chunks;
+  int splits;
+  int chunk;
+  int items;
+  int grid;
+};
+
+// Splits per (b, kv head) when the caller leaves the choice to the library.
+// Work is dealt to persistent CTAs (one per SM) round-robin, so the run
+// time is about the rows on the busiest CTA: ceil(items / SMs) items of
+// `chunk` rows plus a stage of fill/epilogue per item.  When there are fewer
+// items than SMs each active SM can pull more than its even share of HBM
+// bandwidth (modelled as at most 1.5x).  More than one split costs a second
+// launch and a pass over the partials (modelled as 3 us of one SM's streaming).
+int auto_splits(int units, int n_max, int tile, int row_bytes, int sms) {
+  const int max_splits = (n_max + tile - 1) / tile;
+  const double fair_bw_row_per_us = 43.0e3 / double(row_bytes);  // ~43 GB/s per SM
+  const double combine_rows = 3.0 * fair_bw_row_per_us;
+  int best = 1;
+  double best_cost = 1e300;
+  int last_eff = -1;
+  for (int s = 1; s <= max_splits && s <= 4096; ++s) {
+    const int per = (n_max + s - 1) / s;
+    const int chunk = (per + tile - 1) / tile * tile;
+    const int eff = (n_max + chunk - 1) / chunk;
+    if (eff == last_eff) continue;
+    last_eff = eff;
+    const long long items = (long long)units * eff;
+    const long long active = items < sms ? items : sms;
+    const long long rounds = (items + sms - 1) / sms;
+    double speed = double(sms) / double(active);
+    if (speed > 1.5) speed = 1.5;
+    double cost = double(rounds) * double(chunk + tile) / speed;
+    if (eff > 1) cost += combine_rows;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = eff;
+    }
+  }
+  return best;
+}
+
+int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype, int requested, int sms,
+              Plan* pl) {
+  const int group = h_q / h_kv;
+  pl->ks = dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group);
+  pl->head_chunks = (group + pl->ks.heads_per_cta - 1) / pl->ks.heads_per_cta;
+  const int tile = pl->ks.tile_rows;
+  const int max_splits = (n_max + tile - 1) / tile;
+  const int units = B * h_kv * pl->head_chunks;
+  int s = requested;
+  if (s <= 0) {
+    const int es = dtype == DA_BF16 ? 2 : 4;
+    s = auto_splits(units, n_max, tile, 2 * d * es, sms);
+  }
+  if (s > max_splits) s = max_splits;
+  const int per = (n_max + s - 1) / s;
+  pl->chunk = (per + tile - 1) / tile * tile;
+  pl->splits = (n_max + pl->chunk - 1) / pl->chunk;
+  const long long items = (long long)units * pl->splits;
+  if (items > 0x7fffffffLL) return DA_ERR_SHAPE;
+  pl->items = int(items);
+  pl->grid = pl->items < sms ? pl->items : sms;
+  return DA_OK;
+}
+
+size_t workspace_for(const Plan& pl, int B, int h_q, int d) {
+  if (pl.splits <= 1) return 0;
+  return size_t(B) * h_q * pl.splits * (size_t(d) + 1) * sizeof(float);
+}
+
+// Library-owned workspace for decode_attn(), one per device.
+struct OwnedWorkspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+OwnedWorkspace g_ws[kMaxDevices];
+std::mutex g_ws_mu;
+
+}  // namespace
+
+extern "C" {
+
+const char* decode_attn_status_string(int status) {
+  switch (status) {
+    case DA_OK: return "ok";
+    case DA_ERR_NULL: return "null pointer argument";
+    case DA_ERR_SHAPE: return "size out of range or inconsistent";
+    case DA_ERR_DTYPE: return "unknown dtype";
+    case DA_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case DA_ERR_WORKSPACE: return "workspace missing or too small";
+    case DA_ERR_CUDA: return "CUDA call failed";
+    case DA_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+    case DA_ERR_UNSUPPORTED: return "unsupported head dimension combination";
+    default: return "unknown status";
+  }
+}
+
+const char* decode_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t decode_attn_launch_count(void) { return g_launches.load(); }
+
+int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype,
+                               int num_splits) {
+  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype);
+  if (st != DA_OK) return st;
+  int dev, sms;
+  if ((st = current_device(&dev, &sms)) != DA_OK) return st;
+  Plan pl;
+  if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
+  return pl.splits;
+}
+
+size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype,
+                                   int num_splits, int* status) {
+  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype);
+  int dev = 0, sms = 0;
+  Plan pl;
+  if (st == DA_OK) st = current_device(&dev, &sms);
+  if (st == DA_OK) st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl);
+  if (status) *status = st;
+  return st == DA_OK ? workspace_for(pl, B, h_q, d_k) : 0;
+}
+
+int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens, float* out,
+                   int B, int h_q, int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
+                   int num_splits, void* workspace, size_t workspace_bytes, int32_t* dev_error,
+                   cudaStream_t stream) {
+  if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
+  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype);
+  if (st != DA_OK) return st;
+  if (!isfinite(scale)) return DA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return DA_ERR_ALIGN;
+  int dev, sms;
+  if ((st = current_device(&dev, &sms)) != DA_OK) return st;
+  Plan pl;
+  if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
+  const size_t need = workspace_for(pl, B, h_q, d_k);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return DA_ERR_WORKSPACE;
+
+  CUtensorMap tk, tv;
+  if ((st = encode_cache_map(&tk, K, dtype, d_k, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
+  if ((st = encode_cache_map(&tv, V, dtype, d_v, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
+
+  SplitParams p;
+  p.q = q;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = need ? static_cast<float*>(workspace) + size_t(B) * h_q * pl.splits * d_v : nullptr;
+  p.dev_error = dev_error;
+  p.B = B;
+  p.h_q = h_q;
+  p.h_kv = h_kv;
+  p.group = h_q / h_kv;
+  p.n_max = n_max;
+  p.num_splits = pl.splits;
+  p.chunk = pl.chunk;
+  p.head_chunks = pl.head_chunks;
+  p.items = pl.items;
+  p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
+
+  cudaError_t e = dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, pl.grid, stream)
+                                   : da::launch_split_f32(p, tk, tv, d_k, pl.grid, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "split kernel launch");
+  g_launches.fetch_add(1);
+  if (pl.splits > 1) {
+    e = da::launch_combine(p, d_v, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
+    g_launches.fetch_add(1);
+  }
+  return DA_OK;
+}
+
+int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens, float* out,
+                int B, int h_q, int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
+                cudaStream_t stream) {
+  if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
+  int st = DA_OK;
+  const size_t need =
+      decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype, 0, &st);
+  if (st != DA_OK) return st;
+  void* ws = nullptr;
+  // Held through the launch so that a concurrent growth cannot free the
+  // buffer between taking its address and enqueueing the kernels.
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  if (need > 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return DA_ERR_DEVICE;
+    OwnedWorkspace& w = g_ws[dev];
+    if (w.bytes < need) {
+      if (w.ptr) {
+        e = cudaFree(w.ptr);  // waits for work still using the old buffer
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFree(workspace)");
+      }
+      e = cudaMalloc(&w.ptr, need);
+      if (e != cudaSuccess) {
+        w.ptr = nullptr;
+        return fail_cuda(e, "cudaMalloc(workspace)");
+      }
+      w.bytes = need;
+    }
+    ws = w.ptr;
+  }
+  return decode_attn_ex(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype, 0, ws,
+                        need, nullptr, stream);
+}
+
+int kv_append(const void* k_new, const void* v_new, void* K, void* V, const int32_t* pos, int B,
+              int h_kv, int d_k, int d_v, int n_max, int dtype, int32_t* dev_error,
+              cudaStream_t stream) {
+  if (!k_new || !v_new || !K || !V || !pos) return DA_ERR_NULL;
+  if (dtype != DA_FP32 && dtype != DA_BF16) return DA_ERR_DTYPE;
+  if (B <= 0 || h_kv <= 0 || d_k <= 0 || d_v <= 0 || n_max <= 0) return DA_ERR_SHAPE;
+  const int es = dtype == DA_BF16 ? 2 : 4;
+  if ((d_k * es) % 16 != 0 || (d_v * es) % 16 != 0) return DA_ERR_SHAPE;
+  if ((long long)B * h_kv * (long long)n_max > 0x7fffffffLL) return DA_ERR_SHAPE;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(K) || !aligned16(V)) return DA_ERR_ALIGN;
+  int dev, sms;
+  int st = current_device(&dev, &sms);
+  if (st != DA_OK) return st;
+  cudaError_t e = da::launch_kv_append(k_new, v_new, K, V, pos, B, h_kv, d_k * es, d_v * es, n_max,
+                                       dev_error, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "kv_append launch");
+  g_launches.fetch_add(1);
+  return DA_OK;
+}
+
+}  // extern "C"

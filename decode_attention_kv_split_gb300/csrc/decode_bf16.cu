@@ -1,0 +1,447 @@
+// Split-KV decode attention for bf16 caches on tensor cores (sm_103a).
+//
+// One persistent CTA per SM walks a static list of work items
+// (b, kv head, query-head chunk, split).  A producer warp streams the K and
+// V rows of each item through a ring of shared-memory stages with 3-D TMA
+// loads (128-byte swizzle, evict-first L2 policy); consumer warps compute on
+// each stage and hand it back through an mbarrier.  Every K/V byte is read
+// from HBM once per CTA that needs it, and all query heads of a kv head live
+// in the same CTA, so GQA/MQA groups are never broadcast in memory
+// ("MoA-Structured Decode Attention", introduction item 4).
+//
+// Per 16 cached rows a consumer warp computes, for its 8*NB query heads:
+//   Step I  (section 2, eq. 1): S^T = K_rows . Q^T with mma.m16n8k16, the
+//           rows of K as the M operand (16 rows) and the query heads as N
+//           (8 per block), so a group of 8 heads fills the MMA exactly;
+//   Step II (section 2, eq. 2): a running max / running sum (online softmax)
+//           in the log2 domain, exp(x) = 2^(x * log2 e) on the SFU;
+//   Step III(section 2, eq. 3): O^T += V_rows^T . P^T with mma.m16n8k16, the
+//           weights P split into a bf16 head plus a bf16 remainder so they
+//           carry ~16 significant bits into the fp32 accumulators.
+// Rows are read in their natural row-major layout: the K^T of the textbook
+// formula is never formed (section 2, Step I), and lanes run along the
+// contiguous d axis of each row (coalescing criterion of section 4).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace da {
+
+template <int D_, int NB_, int HG_, int KW_, int KBW_, int STAGES_>
+struct Bf16Cfg {
+  static constexpr int D = D_;            // head dim (d_k == d_v)
+  static constexpr int NB = NB_;          // 8-head MMA blocks per warp
+  static constexpr int HG = HG_;          // head groups (warps sharing rows, different heads)
+  static constexpr int KW = KW_;          // key warps per head group
+  static constexpr int KBW = KBW_;        // 16-row blocks per key warp per stage
+  static constexpr int STAGES = STAGES_;
+  static constexpr int kHalves = D / 64;  // 64-column (128-byte) TMA boxes per row
+  static constexpr int kTile = 16 * KW * KBW;
+  static constexpr int kConsumerWarps = HG * KW;
+  static constexpr int kConsumerThreads = 32 * kConsumerWarps;
+  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int kHPW = 8 * NB;            // heads per warp
+  static constexpr int kHeadsPerCta = kHPW * HG;
+  static constexpr int kHalfBytes = kTile * 128;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kSlotStride = D + 4;      // padded row of the epilogue slots
+  static constexpr int kEpiAccFloats = HG * KW * kHPW * kSlotStride;
+  static constexpr int kEpiMLFloats = 2 * HG * KW * kHPW;
+  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * kStageBytes +
+                                       size_t(kEpiAccFloats + kEpiMLFloats) * 4 +
+                                       2 * STAGES * 8 + 16;
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert((kEpiAccFloats + kEpiMLFloats) % 2 == 0, "mbarrier alignment");
+};
+
+// Byte offset of element column `col` (a multiple of 8) of tile row `row`
+// inside one tensor's tile: 64-column halves, 128-byte rows, 128-byte swizzle.
+template <class Cfg>
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  const int half = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return uint32_t(half * Cfg::kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    split_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
+                             const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+  constexpr int D = Cfg::D, NB = Cfg::NB, KW = Cfg::KW, KBW = Cfg::KBW, STAGES = Cfg::STAGES;
+  constexpr int kHPW = Cfg::kHPW;
+  constexpr int MB = D / 16;  // 16-wide blocks of d
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  float* epi_acc = reinterpret_cast<float*>(smem + size_t(STAGES) * Cfg::kStageBytes);
+  float* epi_m = epi_acc + Cfg::kEpiAccFloats;
+  float* epi_l = epi_m + Cfg::HG * KW * kHPW;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_l + Cfg::HG * KW * kHPW);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == Cfg::kConsumerWarps) {
+    if (lane == 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const uint64_t policy = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;        // bit s: stage s has a copy issued
+      uint32_t issued_parity = 0; // bit s: parity of that copy's phase
+      bool aborted = false;
+      for (int i = blockIdx.x; i < p.items && !aborted; i += gridDim.x) {
+        const Item it = decode_item<Cfg::kTile>(p, i, p.dev_error, true);
+        const int z = it.b * p.h_kv + it.kvh;
+        for (int t = 0; t < it.tiles; ++t) {
+          if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+            *abort_flag = 1;
+            flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
+            aborted = true;
+            break;
+          }
+          const uint32_t bar = full0 + 8 * stage;
+          mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+          const uint32_t kdst = ring + stage * Cfg::kStageBytes;
+          const uint32_t vdst = kdst + Cfg::kTileBytes;
+          const int y = it.row_begin + t * Cfg::kTile;
+#pragma unroll
+          for (int h = 0; h < Cfg::kHalves; ++h) {
+            tma_load_3d(kdst + h * Cfg::kHalfBytes, &tmK, h * 64, y, z, bar, policy);
+            tma_load_3d(vdst + h * Cfg::kHalfBytes, &tmV, h * 64, y, z, bar, policy);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        // Let every copy this thread started land before the CTA can exit.
+        volatile int never = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait_bounded(full0 + 8 * s, (issued_parity >> s) & 1u, &never);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int hg = warp / KW;
+  const int kw = warp % KW;
+  const int r = lane >> 2;  // MMA fragment row group
+  const int c = lane & 3;   // MMA fragment column pair
+  const bool single = (p.num_splits == 1);
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+    const Item it = decode_item<Cfg::kTile>(p, i, nullptr, false);
+    if (it.tiles == 0 && !single) continue;  // empty split: the combine skips it
+
+    // Query heads of this warp: group-local index hl = hc*HeadsPerCta + hg*kHPW + nb*8 + n.
+    const int head_base = it.hc * Cfg::kHeadsPerCta + hg * kHPW;
+    uint32_t qf[NB][MB][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const int hl = head_base + nb * 8 + r;
+      const bool ok = hl < p.group;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          static_cast<const __nv_bfloat16*>(p.q) +
+          (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + (ok ? hl : 0)) * D);
+#pragma unroll
+      for (int ks = 0; ks < MB; ++ks) {
+        qf[nb][ks][0] = ok ? __ldg(qrow + ks * 8 + c) : 0u;
+        qf[nb][ks][1] = ok ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+      }
+    }
+
+    float m_run[NB][2], l_run[NB][2];
+    float acc[MB][NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      m_run[nb][0] = m_run[nb][1] = -INFINITY;
+      l_run[nb][0] = l_run[nb][1] = 0.f;
+    }
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mb][nb][e] = 0.f;
+
+    for (int t = 0; t < it.tiles; ++t) {
+      if (!mbar_wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
+        if (!*abort_flag) {
+          *abort_flag = 1;
+          flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
+        }
+      }
+      const uint32_t kbase = ring + stage * Cfg::kStageBytes;
+      const uint32_t vbase = kbase + Cfg::kTileBytes;
+      const int valid = min(Cfg::kTile, it.row_end - (it.row_begin + t * Cfg::kTile));
+      const int key0 = kw * KBW * 16;  // first row of this warp inside the stage
+
+      if (!*abort_flag && key0 < valid) {
+        // ---- Step I: scores for KBW blocks of 16 rows.
+        float s[KBW][NB][4];
+#pragma unroll
+        for (int kb = 0; kb < KBW; ++kb)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[kb][nb][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < MB; ++ks) {
+#pragma unroll
+          for (int kb = 0; kb < KBW; ++kb) {
+            const int row = key0 + kb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int col = ks * 16 + (lane >> 4) * 8;
+            uint32_t a[4];
+            ldmatrix_x4(a, kbase + swz<Cfg>(row, col));
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(s[kb][nb], a, qf[nb][ks][0], qf[nb][ks][1]);
+          }
+        }
+
+        // ---- Step II: mask rows past the end, scale, running max and sum.
+        float alpha[NB][2];
+        bool changed = false;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int kb = 0; kb < KBW; ++kb) {
+              const int row_lo = key0 + kb * 16 + r;
+              s[kb][nb][j] = row_lo < valid ? s[kb][nb][j] * p.scale_log2 : -INFINITY;
+              s[kb][nb][j + 2] = row_lo + 8 < valid ? s[kb][nb][j + 2] * p.scale_log2 : -INFINITY;
+              mx = fmaxf(mx, fmaxf(s[kb][nb][j], s[kb][nb][j + 2]));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[nb][j], mx);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            alpha[nb][j] = ex2(m_run[nb][j] - m_use);
+            changed |= (m_new != m_run[nb][j]);
+            m_run[nb][j] = m_new;
+            float sum = 0.f;
+#pragma unroll
+            for (int kb = 0; kb < KBW; ++kb) {
+              s[kb][nb][j] = ex2(s[kb][nb][j] - m_use);
+              s[kb][nb][j + 2] = ex2(s[kb][nb][j + 2] - m_use);
+              sum += s[kb][nb][j] + s[kb][nb][j + 2];
+            }
+            l_run[nb][j] = l_run[nb][j] * alpha[nb][j] + sum;
+          }
+        }
+        if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              acc[mb][nb][0] *= alpha[nb][0];
+              acc[mb][nb][1] *= alpha[nb][1];
+              acc[mb][nb][2] *= alpha[nb][0];
+              acc[mb][nb][3] *= alpha[nb][1];
+            }
+        }
+
+        // ---- Step III: O^T += V^T . P^T, P as bf16 head + bf16 remainder.
+#pragma unroll
+        for (int kb = 0; kb < KBW; ++kb) {
+          uint32_t ph[NB][2], pl[NB][2];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const uint32_t h0 = pack_bf16x2(s[kb][nb][0], s[kb][nb][1]);  // row r
+            const uint32_t h1 = pack_bf16x2(s[kb][nb][2], s[kb][nb][3]);  // row r + 8
+            const uint32_t l0 = pack_bf16x2(s[kb][nb][0] - bf16_lo_to_f32(h0),
+                                            s[kb][nb][1] - bf16_hi_to_f32(h0));
+            const uint32_t l1 = pack_bf16x2(s[kb][nb][2] - bf16_lo_to_f32(h1),
+                                            s[kb][nb][3] - bf16_hi_to_f32(h1));
+            ph[nb][0] = movmatrix_trans(h0);
+            ph[nb][1] = movmatrix_trans(h1);
+            pl[nb][0] = movmatrix_trans(l0);
+            pl[nb][1] = movmatrix_trans(l1);
+          }
+          const int blk0 = key0 + kb * 16;
+          const bool partial = blk0 + 16 > valid;
+          // rows held by this lane's A registers: {2c, 2c+1} and {8+2c, 9+2c}
+          const uint32_t mlo = (blk0 + 2 * c < valid ? 0x0000ffffu : 0u) |
+                               (blk0 + 2 * c + 1 < valid ? 0xffff0000u : 0u);
+          const uint32_t mhi = (blk0 + 8 + 2 * c < valid ? 0x0000ffffu : 0u) |
+                               (blk0 + 9 + 2 * c < valid ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) {
+            const int row = blk0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+            const int col = mb * 16 + ((lane >> 3) & 1) * 8;
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, vbase + swz<Cfg>(row, col));
+            if (partial) {  // rows past the end may hold anything, even NaN
+              a[0] &= mlo;
+              a[1] &= mlo;
+              a[2] &= mhi;
+              a[3] &= mhi;
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              mma_bf16_16816(acc[mb][nb], a, ph[nb][0], ph[nb][1]);
+              mma_bf16_16816(acc[mb][nb], a, pl[nb][0], pl[nb][1]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+
+    // ---- Epilogue: merge the KW warps of each head group, normalise, store.
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float v = l_run[nb][j];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l_run[nb][j] = v;
+      }
+    named_bar_sync(1, Cfg::kConsumerThreads);  // earlier readers of the slots are done
+    const int slot_id = hg * KW + kw;
+    float* slot = epi_acc + slot_id * kHPW * Cfg::kSlotStride;
+    if (lane < 4) {
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          epi_m[slot_id * kHPW + nb * 8 + 2 * lane + j] = m_run[nb][j];
+          epi_l[slot_id * kHPW + nb * 8 + 2 * lane + j] = l_run[nb][j];
+        }
+    }
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int d0 = mb * 16 + r;
+        const int h0 = nb * 8 + 2 * c;
+        slot[h0 * Cfg::kSlotStride + d0] = acc[mb][nb][0];
+        slot[(h0 + 1) * Cfg::kSlotStride + d0] = acc[mb][nb][1];
+        slot[h0 * Cfg::kSlotStride + d0 + 8] = acc[mb][nb][2];
+        slot[(h0 + 1) * Cfg::kSlotStride + d0 + 8] = acc[mb][nb][3];
+      }
+    named_bar_sync(1, Cfg::kConsumerThreads);
+
+    if (!*abort_flag) {
+      const int tid = kw * 32 + lane;  // thread index inside the head group
+      for (int idx = tid; idx < kHPW * D; idx += KW * 32) {
+        const int hw = idx / D;  // head inside this warp group
+        const int d = idx % D;
+        const int hl = head_base + hw;
+        if (hl >= p.group) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) M = fmaxf(M, epi_m[(hg * KW + k) * kHPW + hw]);
+        float L = 0.f, sum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int k = 0; k < KW; ++k) {
+            const int sid = hg * KW + k;
+            const float f = ex2(epi_m[sid * kHPW + hw] - M);
+            L += f * epi_l[sid * kHPW + hw];
+            sum += f * epi_acc[(sid * kHPW + hw) * Cfg::kSlotStride + d];
+          }
+        }
+        const float o = L > 0.f ? sum / L : 0.f;
+        const size_t bh = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + hl;
+        if (single) {
+          p.out[bh * D + d] = o;
+        } else {
+          p.o_part[(bh * p.num_splits + it.split) * D + d] = o;
+          if (d == 0) p.lse_part[bh * p.num_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Variant table and launcher.
+// ---------------------------------------------------------------------------
+using Bf16G8D128 = Bf16Cfg<128, 1, 1, 4, 2, 3>;
+using Bf16G16D128 = Bf16Cfg<128, 2, 1, 4, 1, 5>;
+using Bf16G32D128 = Bf16Cfg<128, 2, 2, 4, 1, 4>;
+using Bf16G8D64 = Bf16Cfg<64, 1, 1, 4, 2, 6>;
+using Bf16G16D64 = Bf16Cfg<64, 2, 1, 4, 1, 8>;
+using Bf16G32D64 = Bf16Cfg<64, 2, 2, 4, 1, 8>;
+
+template <class Cfg>
+static KernelShape shape_of() {
+  return KernelShape{Cfg::kTile, Cfg::kHeadsPerCta, 64, 1};
+}
+
+KernelShape bf16_shape(int d, int group) {
+  if (d == 128) {
+    if (group <= 8) return shape_of<Bf16G8D128>();
+    if (group <= 16) return shape_of<Bf16G16D128>();
+    return shape_of<Bf16G32D128>();
+  }
+  if (group <= 8) return shape_of<Bf16G8D64>();
+  if (group <= 16) return shape_of<Bf16G16D64>();
+  return shape_of<Bf16G32D64>();
+}
+
+template <class Cfg>
+static cudaError_t launch_cfg(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              int grid, cudaStream_t stream) {
+  static bool attr_done = false;  // benign race: setting the attribute twice is harmless
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(split_decode_bf16_kernel<Cfg>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Cfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  split_decode_bf16_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              int d, int grid, cudaStream_t stream) {
+  if (d == 128) {
+    if (p.group <= 8) return launch_cfg<Bf16G8D128>(p, tk, tv, grid, stream);
+    if (p.group <= 16) return launch_cfg<Bf16G16D128>(p, tk, tv, grid, stream);
+    return launch_cfg<Bf16G32D128>(p, tk, tv, grid, stream);
+  }
+  if (p.group <= 8) return launch_cfg<Bf16G8D64>(p, tk, tv, grid, stream);
+  if (p.group <= 16) return launch_cfg<Bf16G16D64>(p, tk, tv, grid, stream);
+  return launch_cfg<Bf16G32D64>(p, tk, tv, grid, stream);
+}
+
+}  // namespace da

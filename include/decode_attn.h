@@ -1,0 +1,162 @@
+/*
+ * decode_attn: decode-step attention over a KV cache, GB300 (sm_103a).
+ *
+ * C ABI of libdecode_attn.so.  Every entry point takes plain pointers and
+ * sizes.  Device pointers are caller-owned CUDA device memory on the current
+ * device; the library never frees them, never synchronises, and launches all
+ * work asynchronously on the given stream, so buffers must stay alive until
+ * that stream has consumed them.  Every call returns a da_status; when an
+ * argument check fails nothing is launched and no memory is touched.
+ *
+ * What is computed ("MoA-Structured Decode Attention", arXiv 2607.19456):
+ *   for every sequence b and query head h, with kv = h / (h_q / h_kv)
+ *   (GQA/MQA psi-selection, introduction item 4) and n = seq_lens[b]:
+ *     Step I   (section 2, eq. 1)  s[l]  = scale * sum_j q[b,h,j] * K[b,kv,l,j],  l < n
+ *     Step II  (section 2, eq. 2)  a[l]  = exp(s[l] - max s) / sum_l' exp(s[l'] - max s)
+ *     Step III (section 2, eq. 3)  out[b,h,d] = sum_l a[l] * V[b,kv,l,d]
+ *   Tensors are row-major (gamma offsets of section 3):
+ *     q   [B, h_q, d_k]            dtype
+ *     K   [B, h_kv, n_max, d_k]    dtype   (row l of head (b, kv) at ((b*h_kv+kv)*n_max+l)*d_k)
+ *     V   [B, h_kv, n_max, d_v]    dtype
+ *     out [B, h_q, d_v]            float32
+ *   Rows at or beyond seq_lens[b] are never used: they may hold anything,
+ *   including NaN.  A sequence with seq_lens[b] == 0 yields out = 0.
+ *
+ * The softmax is evaluated as a split-KV flash decode: the rows of each
+ * (b, kv head) are cut into num_splits ranges of `chunk` rows, each range
+ * produces a normalised partial output and its log-sum-exp, and a combine
+ * step merges them.  The result equals the definition above up to float
+ * rounding (fp32 accumulation throughout).
+ */
+#ifndef DECODE_ATTN_H_
+#define DECODE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DA_API __attribute__((visibility("default")))
+#else
+#define DA_API
+#endif
+
+/* Element type of q, K, V (and of the rows appended by kv_append). */
+typedef enum {
+  DA_FP32 = 0,
+  DA_BF16 = 1
+} da_dtype;
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_NULL = -1,        /* a required pointer is NULL */
+  DA_ERR_SHAPE = -2,       /* a size is out of range or inconsistent */
+  DA_ERR_DTYPE = -3,       /* unknown dtype */
+  DA_ERR_ALIGN = -4,       /* a device pointer is not 16-byte aligned */
+  DA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
+  DA_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed */
+  DA_ERR_DEVICE = -7,      /* the current device is not sm_103 (GB300) */
+  DA_ERR_UNSUPPORTED = -8  /* valid request this build has no kernel for */
+} da_status;
+
+/* Bits the kernels OR into the optional device error word. */
+#define DA_DEVERR_SEQ_LEN 1 /* some seq_lens[b] outside [0, n_max]: clamped into range */
+#define DA_DEVERR_POS 2     /* some kv_append pos[b] outside [0, n_max): that row not written */
+#define DA_DEVERR_TIMEOUT 4 /* a pipeline wait exceeded its time limit: outputs invalid */
+
+/*
+ * Supported sizes: d_k == d_v, either 64 or 128; any B, h_kv >= 1 and
+ * h_q a multiple of h_kv; 1 <= n_max <= 2^30; B * h_kv * n_max rows must fit
+ * in 2^31 - 1 for the tensor maps.  Alignment: q, K, V, out, k_new, v_new
+ * must be 16-byte aligned.
+ */
+
+/*
+ * Number of splits per (b, kv head) that decode_attn_ex will use for a
+ * request: `num_splits` itself when > 0 (clamped so that every split holds
+ * at least one tile of rows), else the library's choice for the current
+ * device.  Returns a value >= 1, or a negative da_status.
+ */
+DA_API int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                                      int dtype, int num_splits);
+
+/*
+ * Bytes of device workspace decode_attn_ex needs for this request (the
+ * per-split partial outputs and log-sum-exps, float32).  0 when the request
+ * resolves to a single split.  Returns 0 and sets *status (when non-NULL)
+ * to a negative da_status if the arguments are invalid.
+ */
+DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                                          int dtype, int num_splits, int* status);
+
+/*
+ * Decode attention with a caller-provided workspace.
+ *   q, K, V, out : device pointers, layouts above.
+ *   seq_lens     : device int32 [B]; 0 <= seq_lens[b] <= n_max.  Values out
+ *                  of range are clamped and flagged in *dev_error.
+ *   scale        : multiplies q.K (typically 1/sqrt(d_k)).
+ *   num_splits   : splits per (b, kv head); 0 = library's choice.
+ *   workspace    : device memory of at least
+ *                  decode_attn_workspace_bytes(...) bytes, 16-byte aligned;
+ *                  may be NULL when that is 0.  Its contents need no
+ *                  initialisation and are scratch after the call.
+ *   dev_error    : nullable device int32; kernels OR DA_DEVERR_* bits into it
+ *                  (it is never cleared by the library).
+ *   stream       : CUDA stream for every launch.
+ * Launches one split kernel, plus one combine kernel when more than one
+ * split is used.
+ */
+DA_API int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens,
+                          float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                          float scale, int dtype, int num_splits, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream);
+
+/*
+ * Decode attention with a library-owned workspace: the same computation as
+ * decode_attn_ex with num_splits = 0 (library's choice).  The workspace is
+ * cached per device and grown with cudaMalloc when a request needs more (a
+ * growth waits for the device to go idle before freeing the old buffer), so
+ * the first call of a given size must not happen during stream capture.
+ * Concurrent calls on different streams of one device share that workspace
+ * and must be serialised by the caller; use decode_attn_ex otherwise.
+ */
+DA_API int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens,
+                       float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                       float scale, int dtype, cudaStream_t stream);
+
+/*
+ * KV-cache accumulation ("MoA-Structured Decode Attention", introduction
+ * item 3, with the gamma offsets of section 3): for every b < B, h < h_kv
+ *   K[b, h, pos[b], :] = k_new[b, h, :]     (d_k elements)
+ *   V[b, h, pos[b], :] = v_new[b, h, :]     (d_v elements)
+ * as an exact copy of the bits.
+ *   k_new [B, h_kv, d_k], v_new [B, h_kv, d_v] : device, dtype
+ *   K, V  : the caches, written in place
+ *   pos   : device int32 [B], the row to write (normally the current
+ *           seq_lens[b]); a pos outside [0, n_max) writes nothing for that
+ *           sequence and sets DA_DEVERR_POS in *dev_error.
+ * Does not change seq_lens: the caller advances it.
+ */
+DA_API int kv_append(const void* k_new, const void* v_new, void* K, void* V, const int32_t* pos,
+                     int B, int h_kv, int d_k, int d_v, int n_max, int dtype,
+                     int32_t* dev_error, cudaStream_t stream);
+
+/* Static, human-readable name of a da_status. */
+DA_API const char* decode_attn_status_string(int status);
+
+/* Text of the last CUDA error a call on this host thread ran into ("" if none). */
+DA_API const char* decode_attn_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process (all devices). */
+DA_API uint64_t decode_attn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H_ */

@@ -1,0 +1,290 @@
+"""CUDA path against the fp64 CPU oracle, element by element (needs a GB300).
+
+Tolerances (max abs error against the oracle run on the same rounded inputs):
+1e-5 for an fp32 cache, 2e-3 for a bf16 cache; kv_append is bit-exact.
+Cache rows past each sequence's length are filled with NaN, so any read of
+them into a result shows up as a NaN.  Outputs are pre-filled with NaN, so
+any element a kernel fails to write shows up too.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_kv_split_gb300 import api, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-3}
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api.load()
+
+
+def _f32(t):
+    return t.float().contiguous().numpy()
+
+
+def gpu_decode(q, K, V, lens, num_splits=0, scale=None, dev_error=None):
+    dev = torch.device("cuda")
+    qd, Kd, Vd = q.to(dev), K.to(dev), V.to(dev)
+    ld = lens.to(dev)
+    out = torch.full((q.shape[0], q.shape[1], V.shape[3]), float("nan"), device=dev)
+    api.decode_attn(qd, Kd, Vd, ld, out=out, scale=scale, num_splits=num_splits, dev_error=dev_error)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def check_against_oracle(o, q, K, V, lens, scale, out, tol):
+    want, _ = o.decode(_f32(q), _f32(K), _f32(V), lens.numpy(), scale, threads=8)
+    got = out.double().numpy()
+    assert np.all(np.isfinite(got)), "non-finite output (unwritten element or padding read)"
+    err = np.max(np.abs(got - want)) if got.size else 0.0
+    assert err <= tol, f"max abs error {err:.3e} > {tol:.1e}"
+    return err
+
+
+def make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=0, kv_std=1.0):
+    w = W.custom(B=B, h_q=h_q, h_kv=h_kv, d_k=d, n=max(lens) if lens else 0, n_max=n_max,
+                 dtype=dtype, kv_std=kv_std)
+    K, V = W.cache(w, seed)
+    lens_t = torch.tensor(lens, dtype=torch.int32)
+    for b in range(B):
+        K[b, :, lens[b]:] = float("nan")
+        V[b, :, lens[b]:] = float("nan")
+    q = W.query(w, seed)
+    return q, K, V, lens_t, w.scale
+
+
+# ----------------------------------------------------------------- decode sweeps
+SWEEP = [
+    # B, h_q, h_kv, d, n_max, lens
+    (1, 1, 1, 64, 512, [256]),
+    (2, 4, 4, 128, 300, [300, 1]),
+    (3, 8, 2, 128, 200, [200, 0, 77]),
+    (2, 16, 2, 64, 129, [129, 64]),
+    (2, 32, 2, 128, 257, [257, 130]),       # group 16
+    (1, 8, 8, 128, 1000, [999]),
+    (2, 32, 1, 128, 700, [700, 321]),       # MQA group 32
+    (1, 64, 1, 64, 300, [300]),             # group 64 (two head chunks)
+    (2, 12, 4, 128, 385, [385, 129]),       # group 3 (padded heads)
+    (4, 8, 1, 128, 520, [520, 128, 127, 1]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("case", SWEEP, ids=[f"B{c[0]}_hq{c[1]}_hkv{c[2]}_d{c[3]}_n{c[4]}" for c in SWEEP])
+@pytest.mark.parametrize("splits", [0, 1, 3, 1000])
+def test_decode_matches_oracle(o, dtype, case, splits):
+    B, h_q, h_kv, d, n_max, lens = case
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=len(lens) + d)
+    out = gpu_decode(q, K, V, lens_t, num_splits=splits)
+    check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_tile_boundaries(o, dtype):
+    """Lengths one short of, equal to and one past multiples of every stage height."""
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+    for d in (64, 128):
+        for g in (1, 4, 32):
+            q, K, V, lens_t, scale = make_case(len(lens), g, 1, d, 260, lens, dtype, seed=g + d)
+            for splits in (0, 1, 2):
+                out = gpu_decode(q, K, V, lens_t, num_splits=splits)
+                check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_peaked_softmax(o, dtype):
+    """Large scores concentrate the weight on few rows (stresses the P precision)."""
+    q, K, V, lens_t, _ = make_case(2, 8, 2, 128, 400, [400, 37], dtype, seed=3)
+    for scale in (1.0, 0.5):
+        out = gpu_decode(q, K, V, lens_t, scale=scale, num_splits=4)
+        check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
+def test_all_sequences_empty(o):
+    q, K, V, lens_t, scale = make_case(3, 8, 2, 128, 64, [0, 0, 0], torch.bfloat16)
+    for splits in (0, 1, 4):
+        out = gpu_decode(q, K, V, lens_t, num_splits=splits)
+        assert torch.all(out == 0)
+
+
+def test_out_of_range_lengths_are_clamped_and_flagged(o):
+    q, K, V, _, scale = make_case(2, 4, 2, 64, 100, [100, 50], torch.float32)
+    err = torch.zeros((), dtype=torch.int32, device="cuda")
+    bad = torch.tensor([150, -3], dtype=torch.int32)
+    out = gpu_decode(q, K, V, bad, dev_error=err)
+    assert int(err.item()) & api.DEVERR_SEQ_LEN
+    clamped = torch.tensor([100, 0], dtype=torch.int32)
+    check_against_oracle(o, q, K, V, clamped, scale, out, TOL[torch.float32])
+
+
+def test_repeatable_bit_for_bit(o):
+    q, K, V, lens_t, _ = make_case(2, 32, 8, 128, 3000, [3000, 1777], torch.bfloat16)
+    a = gpu_decode(q, K, V, lens_t, num_splits=5)
+    b = gpu_decode(q, K, V, lens_t, num_splits=5)
+    assert torch.equal(a, b)
+
+
+def test_gqa_equals_replicated_mha_on_gpu(o):
+    """Introduction item 4 on the device: reading KV head h // g equals running
+    MHA on a cache with every KV head repeated g times."""
+    for dtype in (torch.float32, torch.bfloat16):
+        q, K, V, lens_t, _ = make_case(2, 16, 4, 128, 300, [300, 200], dtype)
+        a = gpu_decode(q, K, V, lens_t, num_splits=2)
+        Kr = K.repeat_interleave(4, dim=1).contiguous()
+        Vr = V.repeat_interleave(4, dim=1).contiguous()
+        b = gpu_decode(q, Kr, Vr, lens_t, num_splits=2)
+        assert torch.max(torch.abs(a - b)).item() <= TOL[dtype]
+
+
+def test_owned_workspace_entry_point(o):
+    q, K, V, lens_t, scale = make_case(2, 32, 8, 128, 5000, [5000, 4000], torch.bfloat16)
+    dev = torch.device("cuda")
+    out = api.decode_attn_owned(q.to(dev), K.to(dev), V.to(dev), lens_t.to(dev))
+    torch.cuda.synchronize()
+    check_against_oracle(o, q, K, V, lens_t, scale, out.cpu(), TOL[torch.bfloat16])
+
+
+# ----------------------------------------------------------------- kv_append
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_kv_append_bit_exact(o, dtype):
+    B, h_kv, n_max, d = 5, 3, 40, 128
+    w = W.custom(B=B, h_q=h_kv, h_kv=h_kv, d_k=d, n=n_max, n_max=n_max, dtype=dtype)
+    K, V = W.cache(w, 1)
+    kn, vn = W.new_rows(w, 0, 1)
+    pos = torch.tensor([0, 39, 17, -1, 40], dtype=torch.int32)   # last two out of range
+    dev = torch.device("cuda")
+    Kd, Vd = K.to(dev), V.to(dev)
+    err = torch.zeros((), dtype=torch.int32, device=dev)
+    api.kv_append(kn.to(dev), vn.to(dev), Kd, Vd, pos.to(dev), dev_error=err)
+    torch.cuda.synchronize()
+    view = np.uint16 if dtype == torch.bfloat16 else np.uint32
+    Kw = K.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy().view(view).copy()
+    Vw = V.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy().view(view).copy()
+    kw = kn.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy().view(view).copy()
+    vw = vn.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy().view(view).copy()
+    skipped = o.kv_append(kw, vw, Kw, Vw, pos.numpy())
+    assert skipped == 2
+    got_K = Kd.cpu().view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy().view(view)
+    got_V = Vd.cpu().view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy().view(view)
+    assert np.array_equal(got_K, Kw)
+    assert np.array_equal(got_V, Vw)
+    assert int(err.item()) & api.DEVERR_POS
+
+
+def test_append_then_decode_is_causal_last_row(o):
+    """After appending row t, a decode over rows 0..t equals row t of full causal
+    attention computed by the oracle from the same q, k, v rows."""
+    T, d, h = 9, 64, 2
+    rng = np.random.default_rng(7)
+    Q = rng.standard_normal((h, T, d)).astype(np.float32)
+    Kf = rng.standard_normal((h, T, d)).astype(np.float32)
+    Vf = rng.standard_normal((h, T, d)).astype(np.float32)
+    scale = 1 / math.sqrt(d)
+    full = o.causal_attention(Q, Kf, Vf, scale)
+    dev = torch.device("cuda")
+    K = torch.full((1, h, 16, d), float("nan"), device=dev)
+    V = torch.full((1, h, 16, d), float("nan"), device=dev)
+    for t in range(T):
+        pos = torch.tensor([t], dtype=torch.int32, device=dev)
+        api.kv_append(torch.from_numpy(Kf[:, t][None].copy()).to(dev),
+                      torch.from_numpy(Vf[:, t][None].copy()).to(dev), K, V, pos)
+        out = api.decode_attn(torch.from_numpy(Q[:, t][None].copy()).to(dev), K, V, pos + 1)
+        torch.cuda.synchronize()
+        err = np.max(np.abs(out.cpu().double().numpy()[0] - full[:, t]))
+        assert err <= 1e-5, (t, err)
+
+
+# ----------------------------------------------------------------- full-size workloads
+def _sampled_parity(o, w, q, Kd, Vd, lens, out, units):
+    tol = TOL[w.dtype]
+    worst = 0.0
+    for b, h in units:
+        kvh = h // w.group
+        n = int(lens[b])
+        qv = q[b, h].float().numpy()
+        Kb = Kd[b, kvh, :n].float().cpu().numpy()
+        Vb = Vd[b, kvh, :n].float().cpu().numpy()
+        want, _ = o.decode_head(qv, Kb, Vb, w.scale)
+        got = out[b, h].double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        worst = max(worst, float(np.max(np.abs(got - want))))
+    assert worst <= tol, f"{w.name}: max abs error {worst:.3e} > {tol:.1e}"
+
+
+def _units(w, k, seed):
+    rng = np.random.default_rng(seed)
+    picks = {(0, 0), (w.B - 1, w.h_q - 1)}
+    while len(picks) < min(k, w.B * w.h_q):
+        picks.add((int(rng.integers(w.B)), int(rng.integers(w.h_q))))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", ["gqa_llama3_8b", "mqa_g32", "long_llama2_70b"])
+def test_full_size_workload_sampled(o, name):
+    w = W.WORKLOADS[name]
+    dev = torch.device("cuda")
+    K, V = W.cache(w)
+    lens = W.seq_lens(w)
+    q = W.query(w)
+    Kd, Vd = K.to(dev), V.to(dev)
+    del K, V
+    out = torch.full((w.B, w.h_q, w.d_v), float("nan"), device=dev)
+    api.decode_attn(q.to(dev), Kd, Vd, lens.to(dev), out=out, num_splits=w.num_splits)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    _sampled_parity(o, w, q, Kd, Vd, lens, out.cpu(), _units(w, 6, 1))
+
+
+def test_single_head_workload_append_and_redecode(o):
+    w = W.WORKLOADS["single_head"]
+    dev = torch.device("cuda")
+    K, V = W.cache(w, poison=True)
+    lens = W.seq_lens(w)
+    q = W.query(w)
+    Kd, Vd = K.to(dev), V.to(dev)
+    out = gpu_decode(q, K, V, lens)
+    check_against_oracle(o, q, K, V, lens, w.scale, out, TOL[w.dtype])
+    kn, vn = W.new_rows(w, 0)
+    api.kv_append(kn.to(dev), vn.to(dev), Kd, Vd, lens.to(dev))
+    lens2 = lens + 1
+    out2 = torch.full((1, 1, w.d_v), float("nan"), device=dev)
+    api.decode_attn(q.to(dev), Kd, Vd, lens2.to(dev), out=out2)
+    torch.cuda.synchronize()
+    K[0, 0, 256], V[0, 0, 256] = kn[0, 0], vn[0, 0]
+    check_against_oracle(o, q, K, V, lens2, w.scale, out2.cpu(), TOL[w.dtype])
+
+
+def test_mha_fp32_workload_sixteen_steps(o):
+    """All heads, at the first and the last of 16 append+decode steps."""
+    w = W.WORKLOADS["mha_fp32"]
+    dev = torch.device("cuda")
+    K, V = W.cache(w, poison=True)
+    lens = W.seq_lens(w)
+    q = W.query(w)
+    Kd, Vd, ld, qd = K.to(dev), V.to(dev), lens.to(dev), q.to(dev)
+    for t in range(w.steps):
+        kn, vn = W.new_rows(w, t)
+        api.kv_append(kn.to(dev), vn.to(dev), Kd, Vd, ld)
+        ld += 1
+        out = torch.full((w.B, w.h_q, w.d_v), float("nan"), device=dev)
+        api.decode_attn(qd, Kd, Vd, ld, out=out)
+        K[:, :, w.n + t] = kn
+        V[:, :, w.n + t] = vn
+        if t in (0, w.steps - 1):
+            torch.cuda.synchronize()
+            check_against_oracle(o, q, K, V, lens + t + 1, w.scale, out.cpu(), TOL[w.dtype])
+    assert torch.equal(Kd.cpu()[:, :, w.n:w.n + w.steps], K[:, :, w.n:w.n + w.steps])

@@ -39,6 +39,7 @@ SIGNATURES = {
     "decode_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "decode_attn_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
     "decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]),
     "kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "decode_attn_status_string": (ctypes.c_char_p, [_I]),
     "decode_attn_last_cuda_error": (ctypes.c_char_p, []),
@@ -178,6 +179,27 @@ def decode_attn_owned(q, K, V, seq_lens, out=None, scale=None, stream=None) -> t
         st = load().decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q, h_kv,
                                 d_k, d_v, n_max, float(scale), _DTYPES[q.dtype], _stream(q, stream))
     _check(st, "decode_attn")
+    return out
+
+
+def decode_attn_noalloc(q, K, V, seq_lens, out=None, scale=None, num_splits: int = 0,
+                        dev_error=None, stream=None) -> torch.Tensor:
+    """Decode attention through ``decode_attn_noalloc``: the split scratch is the
+    library's own fixed device buffer, so nothing is allocated for it.  Calls
+    whose kernels may overlap on the GPU share that buffer and must be
+    serialised by the caller."""
+    B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    if out is None:
+        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
+    elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
+    with torch.cuda.device(q.device):
+        st = load().decode_attn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q,
+                                        h_kv, d_k, d_v, n_max, float(scale), _DTYPES[q.dtype],
+                                        int(num_splits), _ptr(dev_error), _stream(q, stream))
+    _check(st, "decode_attn_noalloc")
     return out
 
 

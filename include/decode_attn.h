@@ -130,6 +130,36 @@ DA_API int decode_attn(const void* q, const void* K, const void* V, const int32_
                        float scale, int dtype, cudaStream_t stream);
 
 /*
+ * Decode attention that allocates nothing (the pages have no counterpart:
+ * this is a deployment variant of decode_attn_ex).
+ *
+ * For callers that cannot call cudaMalloc: a serving loop where an
+ * allocation would synchronise the device and stall other streams, code
+ * whose device memory is all owned and accounted by another allocator, or a
+ * host runtime with no device allocator at all.  The split partials go to a
+ * scratch buffer of DA_NOALLOC_SCRATCH_BYTES that the library itself holds
+ * as a file-scope device array; every GPU that loads the library keeps it
+ * until the process exits.  Arguments and results are those of
+ * decode_attn_ex; the caller still provides q, K, V, seq_lens and out.
+ *
+ * Returns DA_ERR_WORKSPACE when the request needs more scratch than
+ * DA_NOALLOC_SCRATCH_BYTES (see decode_attn_workspace_bytes; fewer splits
+ * need less).  Calls no cudaMalloc, cudaFree or other allocating routine.
+ * The first call on a device looks up the buffer's device address with that
+ * device current and caches it; make that first call before any stream
+ * capture.  All calls share the one buffer, which keeps the last call's
+ * contents (nothing in it needs to start at zero): calls whose kernels may
+ * overlap on the GPU (different streams, or several host threads) race on it
+ * and must be serialised by the caller.
+ */
+#define DA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+DA_API int decode_attn_noalloc(const void* q, const void* K, const void* V, const int32_t* seq_lens,
+                               float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                               float scale, int dtype, int num_splits, int32_t* dev_error,
+                               cudaStream_t stream);
+
+/*
  * KV-cache accumulation ("MoA-Structured Decode Attention", introduction
  * item 3, with the gamma offsets of section 3): for every b < B, h < h_kv
  *   K[b, h, pos[b], :] = k_new[b, h, :]     (d_k elements)

@@ -382,7 +382,7 @@ def run_ours(args, w, world, rank, local):
         "data": "synthetic", "config": workload_config(wb, n_rot, kv_touch),
         "hbm_gbs": (dec_bytes + app_bytes) / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_of_8tbs": (dec_bytes + app_bytes) / (ms_per_step / 1e3) / 8e12,
-        "decode_ms": decode_ms, "append_ms": append_ms, "num_splits": splits,
+        "decode_ms": decode_ms, "append_ms": append_ms, "max_splits": splits,
         "roofline": {"bound": "hbm", "kernel": "decode_attn (split kernel"
                      + (" + LSE combine)" if splits > 1 else ")"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",

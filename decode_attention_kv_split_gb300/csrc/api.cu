@@ -125,74 +125,62 @@ int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype
 struct Plan {
   KernelShape ks;
   int head_chunks;
-  int splits;
-  int chunk;
-  int items;
-  int grid;
+  int chunk_fixed;     // > 0: rows per split fixed by the caller's num_splits
+  int chunk_min;       // else: the device picks chunk_min * 2^k
+  int max_splits;      // partial slots per query head
+  int batch_per_launch;
 };
 
-// Splits per (b, kv head) when the caller leaves the choice to the library.
-// Work is dealt to persistent CTAs (one per SM) round-robin, so the run
-// time is about the rows on the busiest CTA: ceil(items / SMs) items of
-// `chunk` rows plus a stage of fill/epilogue per item.  When there are fewer
-// items than SMs each active SM can pull more than its even share of HBM
-// bandwidth (modelled as at most 1.5x).  More than one split costs a second
-// launch and a pass over the partials (modelled as 3 us of one SM's streaming).
-int auto_splits(int units, int n_max, int tile, int row_bytes, int sms) {
-  const int max_splits = (n_max + tile - 1) / tile;
-  const double fair_bw_row_per_us = 43.0e3 / double(row_bytes);  // ~43 GB/s per SM
-  const double combine_rows = 3.0 * fair_bw_row_per_us;
-  int best = 1;
-  double best_cost = 1e300;
-  int last_eff = -1;
-  for (int s = 1; s <= max_splits && s <= 4096; ++s) {
-    const int per = (n_max + s - 1) / s;
-    const int chunk = (per + tile - 1) / tile * tile;
-    const int eff = (n_max + chunk - 1) / chunk;
-    if (eff == last_eff) continue;
-    last_eff = eff;
-    const long long items = (long long)units * eff;
-    const long long active = items < sms ? items : sms;
-    const long long rounds = (items + sms - 1) / sms;
-    double speed = double(sms) / double(active);
-    if (speed > 1.5) speed = 1.5;
-    double cost = double(rounds) * double(chunk + tile) / speed;
-    if (eff > 1) cost += combine_rows;
-    if (cost < best_cost * 0.999) {
-      best_cost = cost;
-      best = eff;
-    }
-  }
-  return best;
-}
-
+// Splits per sequence requested by the caller -> a split length that is a
+// whole number of pipeline stages, as close as possible to n_max / S.  When
+// the library chooses, the device picks the length from the actual sequence
+// lengths; the host only bounds it from below so that the partial outputs of
+// at most about 4 x SMs work items per launch need workspace.
 int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype, int requested, int sms,
               Plan* pl) {
   const int group = h_q / h_kv;
   pl->ks = dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group);
   pl->head_chunks = (group + pl->ks.heads_per_cta - 1) / pl->ks.heads_per_cta;
-  const int tile = pl->ks.tile_rows;
-  const int max_splits = (n_max + tile - 1) / tile;
-  const int units = B * h_kv * pl->head_chunks;
-  int s = requested;
-  if (s <= 0) {
-    const int es = dtype == DA_BF16 ? 2 : 4;
-    s = auto_splits(units, n_max, tile, 2 * d * es, sms);
+  pl->batch_per_launch = B < da::kMaxBatchPerLaunch ? B : da::kMaxBatchPerLaunch;
+  const long long tile = pl->ks.tile_rows;
+  const long long max_tiles = (n_max + tile - 1) / tile;
+  if (requested > 0) {
+    long long tiles = (n_max + (long long)requested * tile / 2) / ((long long)requested * tile);
+    if (tiles < 1) tiles = 1;
+    pl->chunk_fixed = int(tiles * tile);
+    pl->chunk_min = pl->chunk_fixed;
+  } else {
+    const long long units = (long long)pl->batch_per_launch * h_kv * pl->head_chunks;
+    long long cap = (4LL * sms + units - 1) / units;
+    if (cap > max_tiles) cap = max_tiles;
+    if (cap < 1) cap = 1;
+    const long long per = (n_max + cap - 1) / cap;
+    pl->chunk_fixed = 0;
+    pl->chunk_min = int((per + tile - 1) / tile * tile);
   }
-  if (s > max_splits) s = max_splits;
-  const int per = (n_max + s - 1) / s;
-  pl->chunk = (per + tile - 1) / tile * tile;
-  pl->splits = (n_max + pl->chunk - 1) / pl->chunk;
-  const long long items = (long long)units * pl->splits;
-  if (items > 0x7fffffffLL) return DA_ERR_SHAPE;
-  pl->items = int(items);
-  pl->grid = pl->items < sms ? pl->items : sms;
+  const long long splits = (n_max + pl->chunk_min - 1) / pl->chunk_min;
+  if (splits >= (1 << 20)) return DA_ERR_SHAPE;
+  pl->max_splits = int(splits);
+  if ((long long)pl->batch_per_launch * h_q * pl->max_splits * (d + 1) > (1LL << 40))
+    return DA_ERR_SHAPE;
   return DA_OK;
 }
 
-size_t workspace_for(const Plan& pl, int B, int h_q, int d) {
-  if (pl.splits <= 1) return 0;
-  return size_t(B) * h_q * pl.splits * (size_t(d) + 1) * sizeof(float);
+// Workspace of one launch: a header word (the split length the kernels
+// used), partial outputs, partial log-sum-exps.
+struct WorkspaceLayout {
+  size_t header, o_part, lse_part, total;
+};
+
+WorkspaceLayout workspace_layout(const Plan& pl, int h_q, int d) {
+  WorkspaceLayout w{0, 0, 0, 0};
+  if (pl.max_splits <= 1) return w;
+  const size_t heads = size_t(pl.batch_per_launch) * h_q;
+  w.header = 0;
+  w.o_part = 256;
+  w.lse_part = w.o_part + heads * pl.max_splits * d * sizeof(float);
+  w.total = w.lse_part + heads * pl.max_splits * sizeof(float);
+  return w;
 }
 
 // Library-owned workspace for decode_attn(), one per device.
@@ -234,7 +222,7 @@ int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v, int n
   if ((st = current_device(&dev, &sms)) != DA_OK) return st;
   Plan pl;
   if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
-  return pl.splits;
+  return pl.max_splits;
 }
 
 size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype,
@@ -245,7 +233,7 @@ size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, i
   if (st == DA_OK) st = current_device(&dev, &sms);
   if (st == DA_OK) st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl);
   if (status) *status = st;
-  return st == DA_OK ? workspace_for(pl, B, h_q, d_k) : 0;
+  return st == DA_OK ? workspace_layout(pl, h_q, d_k).total : 0;
 }
 
 int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens, float* out,
@@ -263,39 +251,48 @@ int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* s
   if ((st = current_device(&dev, &sms)) != DA_OK) return st;
   Plan pl;
   if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
-  const size_t need = workspace_for(pl, B, h_q, d_k);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return DA_ERR_WORKSPACE;
+  const WorkspaceLayout wl = workspace_layout(pl, h_q, d_k);
+  if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return DA_ERR_WORKSPACE;
 
   CUtensorMap tk, tv;
   if ((st = encode_cache_map(&tk, K, dtype, d_k, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
   if ((st = encode_cache_map(&tv, V, dtype, d_v, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
 
-  SplitParams p;
-  p.q = q;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.o_part = static_cast<float*>(workspace);
-  p.lse_part = need ? static_cast<float*>(workspace) + size_t(B) * h_q * pl.splits * d_v : nullptr;
-  p.dev_error = dev_error;
-  p.B = B;
-  p.h_q = h_q;
-  p.h_kv = h_kv;
-  p.group = h_q / h_kv;
-  p.n_max = n_max;
-  p.num_splits = pl.splits;
-  p.chunk = pl.chunk;
-  p.head_chunks = pl.head_chunks;
-  p.items = pl.items;
-  p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
-
-  cudaError_t e = dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, pl.grid, stream)
-                                   : da::launch_split_f32(p, tk, tv, d_k, pl.grid, stream);
-  if (e != cudaSuccess) return fail_cuda(e, "split kernel launch");
-  g_launches.fetch_add(1);
-  if (pl.splits > 1) {
-    e = da::launch_combine(p, d_v, stream);
-    if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
+  const int es = dtype == DA_BF16 ? 2 : 4;
+  char* ws = static_cast<char*>(workspace);
+  for (int b0 = 0; b0 < B; b0 += pl.batch_per_launch) {
+    const int bn = (B - b0) < pl.batch_per_launch ? (B - b0) : pl.batch_per_launch;
+    SplitParams p;
+    p.q = static_cast<const char*>(q) + size_t(b0) * h_q * d_k * es;
+    p.seq_lens = seq_lens + b0;
+    p.out = out + size_t(b0) * h_q * d_v;
+    p.o_part = wl.total ? reinterpret_cast<float*>(ws + wl.o_part) : nullptr;
+    p.lse_part = wl.total ? reinterpret_cast<float*>(ws + wl.lse_part) : nullptr;
+    p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
+    p.dev_error = dev_error;
+    p.B = bn;
+    p.h_q = h_q;
+    p.h_kv = h_kv;
+    p.group = h_q / h_kv;
+    p.b_offset = b0;
+    p.n_max = n_max;
+    p.head_chunks = pl.head_chunks;
+    p.chunk_fixed = pl.chunk_fixed;
+    p.chunk_min = pl.chunk_min;
+    p.max_splits = pl.max_splits;
+    p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
+    const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
+    const int grid = int(items < sms ? items : sms);
+    cudaError_t err = dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
+                                       : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
+    if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
+    if (wl.total) {
+      err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.out, bn, h_q, d_v,
+                               pl.max_splits, n_max, stream);
+      if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
+      g_launches.fetch_add(1);
+    }
   }
   return DA_OK;
 }

@@ -15,22 +15,28 @@
 namespace da {
 
 // ---------------------------------------------------------------------------
-// Launch parameters shared by the split kernels and the combine kernel.
+// Launch parameters shared by the split kernels.
 // ---------------------------------------------------------------------------
+// Sequences per launch: the work list is built in shared memory from this many
+// lengths; the host cuts larger batches into several launches.
+constexpr int kMaxBatchPerLaunch = 512;
+
 struct SplitParams {
-  const void* q;            // [B, h_q, d]
-  const int32_t* seq_lens;  // [B]
-  float* out;               // [B, h_q, d] (written when num_splits == 1)
-  float* o_part;            // [B, h_q, num_splits, d]   (num_splits > 1)
-  float* lse_part;          // [B, h_q, num_splits]      log2-domain lse
-  int32_t* dev_error;       // nullable
-  int B, h_q, h_kv, group;  // group = h_q / h_kv
+  const void* q;                 // [B, h_q, d]  (this launch's slice of the batch)
+  const int32_t* seq_lens;       // [B]
+  float* out;                    // [B, h_q, d]
+  float* o_part;                 // [B, h_q, max_splits, d]  normalised partial outputs
+  float* lse_part;               // [B, h_q, max_splits]     log2-domain log-sum-exp
+  int* chunk_out;                // workspace word receiving the split length used (nullable)
+  int32_t* dev_error;            // nullable
+  int B, h_q, h_kv, group;       // group = h_q / h_kv
+  int b_offset;                  // first sequence of this launch inside the tensor maps
   int n_max;
-  int num_splits;           // S: splits per (b, kv head)
-  int chunk;                // C: rows per split (multiple of the tile height)
-  int head_chunks;          // query-head chunks per kv head
-  int items;                // B * h_kv * head_chunks * num_splits
-  float scale_log2;         // scale * log2(e)
+  int head_chunks;               // query-head chunks per kv head
+  int chunk_fixed;               // > 0: rows per split chosen by the caller
+  int chunk_min;                 // else: smallest rows per split the device may choose
+  int max_splits;                // partial slots per query head (ceil(n_max / chunk))
+  float scale_log2;              // scale * log2(e)
 };
 
 // Wall-clock limit for any wait inside a kernel.  A pipeline wait that has
@@ -104,6 +110,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Contiguous bulk copy global -> shared (size a multiple of 16 bytes, both
+// addresses 16-byte aligned), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -190,41 +207,313 @@ cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const
                               int d, int grid, cudaStream_t stream);
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
-cudaError_t launch_combine(const SplitParams& p, int d, cudaStream_t stream);
+cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
+                           const int32_t* seq_lens, float* out, int B, int h_q, int d,
+                           int max_splits, int n_max, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void* V,
                              const int32_t* pos, int B, int h_kv, int row_bytes_k,
                              int row_bytes_v, int n_max, int32_t* dev_error, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
-// Work items: (b, kv head, head chunk, split), split fastest.
+// Work list.
+//
+// Sequence b is cut into nv_b = max(1, ceil(n_b / chunk)) splits of `chunk`
+// rows.  Each (kv head, head chunk) of b is a unit; each (unit, split) is a
+// work item.  Items are numbered sequence by sequence, unit by unit, split by
+// split, so the splits of one unit are consecutive and units complete one
+// after another.  Persistent CTAs take items i = blockIdx.x + k * gridDim.x.
+// Every CTA builds the same list in shared memory from seq_lens.
 // ---------------------------------------------------------------------------
+struct Schedule {
+  int* first;       // [B + 1] first item of sequence b (shared memory)
+  int* lens;        // [B] clamped lengths (shared memory)
+  int chunk;
+  int total;
+};
+
 struct Item {
-  int b, kvh, hc, split;
-  int row_begin, row_end;  // rows [row_begin, row_end) of this (b, kvh); empty if equal
+  int b, kvh, hc, split, nv;
+  int row_begin, row_end;  // rows [row_begin, row_end) of head (b, kvh)
   int tiles;
 };
 
 template <int TILE>
-__device__ __forceinline__ Item decode_item(const SplitParams& p, int i, int32_t* err_sink,
-                                            bool report) {
-  Item it;
-  it.split = i % p.num_splits;
-  int rest = i / p.num_splits;
-  it.hc = rest % p.head_chunks;
-  rest /= p.head_chunks;
-  it.kvh = rest % p.h_kv;
-  it.b = rest / p.h_kv;
-  int n = __ldg(p.seq_lens + it.b);
-  if (n < 0 || n > p.n_max) {
-    if (report) flag_error(err_sink, DA_DEVERR_SEQ_LEN);
-    n = n < 0 ? 0 : p.n_max;
+__device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedule& s, int i) {
+  // last b with first[b] <= i
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.first[mid] <= i) lo = mid; else hi = mid - 1;
   }
-  it.row_begin = it.split * p.chunk;
-  int end = it.row_begin + p.chunk;
+  Item it;
+  it.b = lo;
+  const int per_seq = p.h_kv * p.head_chunks;
+  it.nv = (s.first[lo + 1] - s.first[lo]) / per_seq;
+  const int r = i - s.first[lo];
+  const int unit = r / it.nv;
+  it.split = r - unit * it.nv;
+  it.kvh = unit / p.head_chunks;
+  it.hc = unit - it.kvh * p.head_chunks;
+  const int n = s.lens[lo];
+  it.row_begin = it.split * s.chunk;
+  const int end = it.row_begin + s.chunk;
   it.row_end = end < n ? end : n;
   if (it.row_end < it.row_begin) it.row_end = it.row_begin;
   it.tiles = (it.row_end - it.row_begin + TILE - 1) / TILE;
   return it;
+}
+
+// Choose the split length when the caller left it to the library.  Candidates
+// are chunk_min * 2^k up to the first one covering the longest sequence.  For
+// each, the estimated time in "rows streamed by one CTA" is the larger of the
+// even share of all rows and the busiest CTA's rows (CTAs take items
+// round-robin; a CTA alone can stream ~1.6x its even share of HBM
+// bandwidth), plus one tile of epilogue per item and two tiles when partials
+// must be merged.  Warp 0 does the work (lane k scores candidate k, using
+// ceil(n / (a * 2^k)) = ceil(ceil(n / a) / 2^k)); all threads call this.
+__device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* lens, int tile,
+                                            int grid, int* red /* shared, >= 1 int */) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int lane = tid;
+    unsigned cnt[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) cnt[k] = 0;
+    long long rows = 0;
+    int nmax = 0;
+    for (int b = lane; b < p.B; b += 32) {
+      const int n = lens[b];
+      rows += n;
+      nmax = n > nmax ? n : nmax;
+      const unsigned u = n <= 0 ? 1u : unsigned((n + p.chunk_min - 1) / p.chunk_min);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const unsigned c = k < 31 ? (u + (1u << k) - 1u) >> k : 1u;
+        cnt[k] += c > 0u ? c : 1u;
+      }
+    }
+    // lane k ends up with the total for candidate k
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      unsigned v = cnt[k];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == k) cnt[0] = v;
+    }
+    const unsigned total_k = cnt[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      rows += __shfl_xor_sync(0xffffffffu, rows, o);
+      nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
+    }
+    const long long longest = nmax > 0 ? nmax : 1;
+    const int k = lane;
+    const long long c = (long long)p.chunk_min << k;
+    const long long cprev = k == 0 ? 0 : ((long long)p.chunk_min << (k - 1));
+    const bool candidate = k < 31 && cprev < longest;  // stop after the first covering one
+    float t = 3.0e38f;
+    if (candidate) {
+      const int per_seq = p.h_kv * p.head_chunks;
+      const float items = float(total_k) * float(per_seq);
+      const float rounds = ceilf(items / float(grid));
+      const float share = float(rows) * float(per_seq) / float(grid);
+      const float ceff = float(c < longest ? c : longest);
+      t = fmaxf(share, rounds * ceff * (1.f / 1.6f)) + rounds * float(tile);
+      if (c < longest) t += 2.f * float(tile);
+    }
+    // argmin over lanes, ties (within 0.1%) to the smaller k (fewer items)
+    int best_k = k;
+    float best_t = t;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+      const int ok = __shfl_xor_sync(0xffffffffu, best_k, o);
+      const bool take = ok < best_k ? ot <= best_t * 1.001f : ot * 1.001f < best_t;
+      if (take) {
+        best_t = ot;
+        best_k = ok;
+      }
+    }
+    if (lane == 0) red[0] = int((long long)p.chunk_min << best_k);
+  }
+  __syncthreads();
+  const int chunk = red[0];
+  __syncthreads();
+  return chunk;
+}
+
+// Builds the work list in shared memory; every thread of the CTA must call it.
+// `first` has room for kMaxBatchPerLaunch + 1 ints, `lens` for kMaxBatchPerLaunch,
+// `red` for 48 ints.
+template <int TILE>
+__device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* first, int* lens,
+                                                   int* red) {
+  const int tid = threadIdx.x;
+  bool bad = false;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    int n = __ldg(p.seq_lens + b);
+    if (n < 0 || n > p.n_max) {
+      bad = true;
+      n = n < 0 ? 0 : p.n_max;
+    }
+    lens[b] = n;
+  }
+  if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
+  __syncthreads();
+  Schedule s;
+  s.first = first;
+  s.lens = lens;
+  s.chunk = p.chunk_fixed > 0 ? p.chunk_fixed : choose_chunk(p, lens, TILE, gridDim.x, red);
+  // exclusive scan of items per sequence by warp 0
+  const int per_seq = p.h_kv * p.head_chunks;
+  if (tid < 32) {
+    int carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + tid;
+      int c = 0;
+      if (b < p.B) {
+        const int n = lens[b];
+        c = per_seq * (n <= 0 ? 1 : (n + s.chunk - 1) / s.chunk);
+      }
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (tid >= o) x += y;
+      }
+      if (b < p.B) first[b] = carry + x - c;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (tid == 0) first[p.B] = carry;
+  }
+  __syncthreads();
+  s.total = first[p.B];
+  if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = s.chunk;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// End of a work item, shared by every split kernel.
+//
+// The consumer warps have written, per (key warp, head), their running max m
+// (log2 domain), running sum l and unnormalised accumulator into shared
+// slots.  This merges the KW key warps of each head group by log-sum-exp and
+// writes the item's normalised output: straight to `out` when the sequence
+// has a single split, else to its partial slot with its log-sum-exp for the
+// combine kernel.  All consumer threads call it together.
+// ---------------------------------------------------------------------------
+template <int D, int HG, int KW, int HPW, int SLOT_STRIDE>
+__device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it,
+                                            const float* epi_acc, const float* epi_m,
+                                            const float* epi_l, int ctid, int nthreads,
+                                            volatile int* abort_flag) {
+  constexpr int GC = HG * HPW;  // query heads of this item
+  if (*abort_flag) return;
+  const int head0 = it.hc * GC;  // group-local index of the item's first head
+  const size_t bh0 = (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group);
+  for (int idx = ctid; idx < GC * D; idx += nthreads) {
+    const int h = idx / D;  // head inside the item
+    const int d = idx - h * D;
+    if (head0 + h >= p.group) continue;
+    const int hg = h / HPW, hw = h - hg * HPW;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < KW; ++k) M = fmaxf(M, epi_m[(hg * KW + k) * HPW + hw]);
+    float L = 0.f, sum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < KW; ++k) {
+        const int sid = hg * KW + k;
+        const float f = ex2(epi_m[sid * HPW + hw] - M);
+        L += f * epi_l[sid * HPW + hw];
+        sum += f * epi_acc[(sid * HPW + hw) * SLOT_STRIDE + d];
+      }
+    }
+    const float o = L > 0.f ? sum / L : 0.f;
+    const size_t bh = bh0 + head0 + h;
+    if (it.nv == 1) {
+      p.out[bh * D + d] = o;
+    } else {
+      p.o_part[(bh * p.max_splits + it.split) * D + d] = o;
+      if (d == 0) p.lse_part[bh * p.max_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
+    }
+  }
+}
+
+// Let a combine kernel launched with programmatic stream serialisation start
+// its launch while this grid is still running (it waits for our completion).
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// In a dependent grid: wait until the preceding grid has completed and its
+// memory operations are visible.
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Producer: one thread streams every tile of the CTA's items into the ring.
+// NBOX boxes of BOX_COLS columns per tensor per stage, each BOX_BYTES long.
+// ---------------------------------------------------------------------------
+// The query rows of an item (its head chunk of one kv group, contiguous in
+// q) ride with the item's first stage into that stage's q slot.
+template <int TILE, int STAGES, int STAGE_BYTES, int NBOX, int BOX_COLS, int BOX_BYTES,
+          int HEADS, int ROW_BYTES>
+__device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                        const SplitParams& p, const Schedule& s, uint32_t ring,
+                                        uint32_t qslots, uint32_t full0, uint32_t empty0,
+                                        volatile int* abort_flag) {
+  prefetch_tmap(tmK);
+  prefetch_tmap(tmV);
+  const uint64_t policy = l2_policy_evict_first();
+  constexpr int kTileBytes = STAGE_BYTES / 2;
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, issued_parity = 0;
+  bool aborted = false;
+  for (int i = blockIdx.x; i < s.total && !aborted; i += gridDim.x) {
+    const Item it = schedule_item<TILE>(p, s, i);
+    const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
+    for (int t = 0; t < it.tiles; ++t) {
+      if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+        *abort_flag = 1;
+        flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      const uint32_t bar = full0 + 8 * stage;
+      if (t == 0) {
+        const int h0 = it.hc * HEADS;
+        const int nh = min(HEADS, p.group - h0);
+        const uint32_t qbytes = uint32_t(nh) * ROW_BYTES;
+        mbar_arrive_expect_tx(bar, STAGE_BYTES + qbytes);
+        const char* qsrc = static_cast<const char*>(p.q) +
+                           (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * ROW_BYTES;
+        bulk_load(qslots + stage * (HEADS * ROW_BYTES), qsrc, qbytes, bar);
+      } else {
+        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+      }
+      const uint32_t kdst = ring + stage * STAGE_BYTES;
+      const int y = it.row_begin + t * TILE;
+#pragma unroll
+      for (int h = 0; h < NBOX; ++h) {
+        tma_load_3d(kdst + h * BOX_BYTES, tmK, h * BOX_COLS, y, z, bar, policy);
+        tma_load_3d(kdst + kTileBytes + h * BOX_BYTES, tmV, h * BOX_COLS, y, z, bar, policy);
+      }
+      issued |= 1u << stage;
+      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (aborted) {
+    // Let every copy this thread started land before the CTA can exit.
+    volatile int never = 0;
+    for (int st = 0; st < STAGES; ++st)
+      if (issued & (1u << st)) mbar_wait_bounded(full0 + 8 * st, (issued_parity >> st) & 1u, &never);
+  }
 }
 
 }  // namespace da

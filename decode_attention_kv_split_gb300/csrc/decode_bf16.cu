@@ -48,8 +48,12 @@ struct Bf16Cfg {
   static constexpr int kSlotStride = D + 4;      // padded row of the epilogue slots
   static constexpr int kEpiAccFloats = HG * KW * kHPW * kSlotStride;
   static constexpr int kEpiMLFloats = 2 * HG * KW * kHPW;
-  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * kStageBytes +
-                                       size_t(kEpiAccFloats + kEpiMLFloats) * 4 +
+  // schedule: first[kMaxBatchPerLaunch + 1], lens[kMaxBatchPerLaunch], red[48]
+  // (rounded up to an even count of 4-byte words)
+  static constexpr int kSchedWords = (2 * kMaxBatchPerLaunch + 1 + 48 + 1) & ~1;
+  static constexpr int kQBytes = kHeadsPerCta * D * 2;  // q rows of one item, per stage
+  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes) +
+                                       size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 +
                                        2 * STAGES * 8 + 16;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -76,10 +80,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* epi_acc = reinterpret_cast<float*>(smem + size_t(STAGES) * Cfg::kStageBytes);
+  uint8_t* qslots = smem + size_t(STAGES) * Cfg::kStageBytes;
+  float* epi_acc = reinterpret_cast<float*>(qslots + size_t(STAGES) * Cfg::kQBytes);
   float* epi_m = epi_acc + Cfg::kEpiAccFloats;
   float* epi_l = epi_m + Cfg::HG * KW * kHPW;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_l + Cfg::HG * KW * kHPW);
+  int* sched_first = reinterpret_cast<int*>(epi_l + Cfg::HG * KW * kHPW);
+  int* sched_lens = sched_first + kMaxBatchPerLaunch + 1;
+  int* sched_red = sched_lens + kMaxBatchPerLaunch;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sched_first + Cfg::kSchedWords);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
   const uint32_t ring = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
@@ -96,54 +104,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  const Schedule sched = build_schedule<Cfg::kTile>(p, sched_first, sched_lens, sched_red);
+  allow_dependent_launch();
 
   // ------------------------------------------------------------------ producer
   if (warp == Cfg::kConsumerWarps) {
-    if (lane == 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      const uint64_t policy = l2_policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0;        // bit s: stage s has a copy issued
-      uint32_t issued_parity = 0; // bit s: parity of that copy's phase
-      bool aborted = false;
-      for (int i = blockIdx.x; i < p.items && !aborted; i += gridDim.x) {
-        const Item it = decode_item<Cfg::kTile>(p, i, p.dev_error, true);
-        const int z = it.b * p.h_kv + it.kvh;
-        for (int t = 0; t < it.tiles; ++t) {
-          if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
-            *abort_flag = 1;
-            flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
-            aborted = true;
-            break;
-          }
-          const uint32_t bar = full0 + 8 * stage;
-          mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
-          const uint32_t kdst = ring + stage * Cfg::kStageBytes;
-          const uint32_t vdst = kdst + Cfg::kTileBytes;
-          const int y = it.row_begin + t * Cfg::kTile;
-#pragma unroll
-          for (int h = 0; h < Cfg::kHalves; ++h) {
-            tma_load_3d(kdst + h * Cfg::kHalfBytes, &tmK, h * 64, y, z, bar, policy);
-            tma_load_3d(vdst + h * Cfg::kHalfBytes, &tmV, h * 64, y, z, bar, policy);
-          }
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (aborted) {
-        // Let every copy this thread started land before the CTA can exit.
-        volatile int never = 0;
-        for (int s = 0; s < STAGES; ++s)
-          if (issued & (1u << s)) mbar_wait_bounded(full0 + 8 * s, (issued_parity >> s) & 1u, &never);
-      }
-    }
+    if (lane == 0)
+      produce<Cfg::kTile, STAGES, Cfg::kStageBytes, Cfg::kHalves, 64, Cfg::kHalfBytes,
+              Cfg::kHeadsPerCta, D * 2>(&tmK, &tmV, p, sched, ring, smem_u32(qslots), full0,
+                                        empty0, abort_flag);
     return;
   }
 
@@ -152,30 +121,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const int kw = warp % KW;
   const int r = lane >> 2;  // MMA fragment row group
   const int c = lane & 3;   // MMA fragment column pair
-  const bool single = (p.num_splits == 1);
   int stage = 0;
   uint32_t phase = 0;
 
-  for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
-    const Item it = decode_item<Cfg::kTile>(p, i, nullptr, false);
-    if (it.tiles == 0 && !single) continue;  // empty split: the combine skips it
+  for (int i = blockIdx.x; i < sched.total; i += gridDim.x) {
+    const Item it = schedule_item<Cfg::kTile>(p, sched, i);
 
     // Query heads of this warp: group-local index hl = hc*HeadsPerCta + hg*kHPW + nb*8 + n.
+    // Their bf16 rows arrive with the item's first stage (rows past the group are zero).
     const int head_base = it.hc * Cfg::kHeadsPerCta + hg * kHPW;
     uint32_t qf[NB][MB][2];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int hl = head_base + nb * 8 + r;
-      const bool ok = hl < p.group;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          static_cast<const __nv_bfloat16*>(p.q) +
-          (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + (ok ? hl : 0)) * D);
-#pragma unroll
-      for (int ks = 0; ks < MB; ++ks) {
-        qf[nb][ks][0] = ok ? __ldg(qrow + ks * 8 + c) : 0u;
-        qf[nb][ks][1] = ok ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
-      }
-    }
 
     float m_run[NB][2], l_run[NB][2];
     float acc[MB][NB][4];
@@ -202,6 +157,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t vbase = kbase + Cfg::kTileBytes;
       const int valid = min(Cfg::kTile, it.row_end - (it.row_begin + t * Cfg::kTile));
       const int key0 = kw * KBW * 16;  // first row of this warp inside the stage
+      if (t == 0) {
+        const uint32_t* qs =
+            reinterpret_cast<const uint32_t*>(qslots + size_t(stage) * Cfg::kQBytes);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const int hloc = hg * kHPW + nb * 8 + r;  // head inside the item
+          const bool ok = head_base + nb * 8 + r < p.group;
+#pragma unroll
+          for (int ks = 0; ks < MB; ++ks) {
+            qf[nb][ks][0] = ok ? qs[hloc * (D / 2) + ks * 8 + c] : 0u;
+            qf[nb][ks][1] = ok ? qs[hloc * (D / 2) + ks * 8 + 4 + c] : 0u;
+          }
+        }
+      }
 
       if (!*abort_flag && key0 < valid) {
         // ---- Step I: scores for KBW blocks of 16 rows.
@@ -322,7 +291,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
     }
 
-    // ---- Epilogue: merge the KW warps of each head group, normalise, store.
+    // ---- Epilogue: per-warp state to shared slots, then the shared finish.
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
@@ -357,37 +326,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         slot[(h0 + 1) * Cfg::kSlotStride + d0 + 8] = acc[mb][nb][3];
       }
     named_bar_sync(1, Cfg::kConsumerThreads);
-
-    if (!*abort_flag) {
-      const int tid = kw * 32 + lane;  // thread index inside the head group
-      for (int idx = tid; idx < kHPW * D; idx += KW * 32) {
-        const int hw = idx / D;  // head inside this warp group
-        const int d = idx % D;
-        const int hl = head_base + hw;
-        if (hl >= p.group) continue;
-        float M = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < KW; ++k) M = fmaxf(M, epi_m[(hg * KW + k) * kHPW + hw]);
-        float L = 0.f, sum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int k = 0; k < KW; ++k) {
-            const int sid = hg * KW + k;
-            const float f = ex2(epi_m[sid * kHPW + hw] - M);
-            L += f * epi_l[sid * kHPW + hw];
-            sum += f * epi_acc[(sid * kHPW + hw) * Cfg::kSlotStride + d];
-          }
-        }
-        const float o = L > 0.f ? sum / L : 0.f;
-        const size_t bh = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + hl;
-        if (single) {
-          p.out[bh * D + d] = o;
-        } else {
-          p.o_part[(bh * p.num_splits + it.split) * D + d] = o;
-          if (d == 0) p.lse_part[bh * p.num_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
-        }
-      }
-    }
+    finish_item<D, Cfg::HG, KW, kHPW, Cfg::kSlotStride>(p, it, epi_acc, epi_m, epi_l, threadIdx.x,
+                                                        Cfg::kConsumerThreads, abort_flag);
   }
 }
 
@@ -396,7 +336,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 // ---------------------------------------------------------------------------
 using Bf16G8D128 = Bf16Cfg<128, 1, 1, 4, 2, 3>;
 using Bf16G16D128 = Bf16Cfg<128, 2, 1, 4, 1, 5>;
-using Bf16G32D128 = Bf16Cfg<128, 2, 2, 4, 1, 4>;
+using Bf16G32D128 = Bf16Cfg<128, 2, 2, 2, 2, 4>;
 using Bf16G8D64 = Bf16Cfg<64, 1, 1, 4, 2, 6>;
 using Bf16G16D64 = Bf16Cfg<64, 2, 1, 4, 1, 8>;
 using Bf16G32D64 = Bf16Cfg<64, 2, 2, 4, 1, 8>;

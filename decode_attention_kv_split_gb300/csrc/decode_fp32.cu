@@ -34,9 +34,12 @@ struct F32Cfg {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kEpiAccFloats = W * G * D;
   static constexpr int kEpiMLFloats = 2 * W * G;
-  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * kStageBytes +
-                                       size_t(kEpiAccFloats + kEpiMLFloats) * 4 +
+  static constexpr int kSchedWords = (2 * kMaxBatchPerLaunch + 1 + 48 + 1) & ~1;
+  static constexpr int kQBytes = G * D * 4;  // q rows of one item, per stage
+  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes) +
+                                       size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 +
                                        2 * STAGES * 8 + 16;
+  static_assert((kEpiAccFloats + kEpiMLFloats) % 2 == 0, "mbarrier alignment");
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kTile % W == 0, "rows per warp");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -63,10 +66,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* epi_acc = reinterpret_cast<float*>(smem + size_t(STAGES) * Cfg::kStageBytes);
+  uint8_t* qslots = smem + size_t(STAGES) * Cfg::kStageBytes;
+  float* epi_acc = reinterpret_cast<float*>(qslots + size_t(STAGES) * Cfg::kQBytes);
   float* epi_m = epi_acc + Cfg::kEpiAccFloats;
   float* epi_l = epi_m + W * G;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_l + W * G);
+  int* sched_first = reinterpret_cast<int*>(epi_l + W * G);
+  int* sched_lens = sched_first + kMaxBatchPerLaunch + 1;
+  int* sched_red = sched_lens + kMaxBatchPerLaunch;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sched_first + Cfg::kSchedWords);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
   const uint32_t ring = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
@@ -83,77 +90,28 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
+  const Schedule sched = build_schedule<Cfg::kTile>(p, sched_first, sched_lens, sched_red);
+  allow_dependent_launch();
 
   // ------------------------------------------------------------------ producer
   if (warp == W) {
-    if (lane == 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      const uint64_t policy = l2_policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, issued_parity = 0;
-      bool aborted = false;
-      for (int i = blockIdx.x; i < p.items && !aborted; i += gridDim.x) {
-        const Item it = decode_item<Cfg::kTile>(p, i, p.dev_error, true);
-        const int z = it.b * p.h_kv + it.kvh;
-        for (int t = 0; t < it.tiles; ++t) {
-          if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
-            *abort_flag = 1;
-            flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
-            aborted = true;
-            break;
-          }
-          const uint32_t bar = full0 + 8 * stage;
-          mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
-          const uint32_t kdst = ring + stage * Cfg::kStageBytes;
-          const int y = it.row_begin + t * Cfg::kTile;
-          tma_load_3d(kdst, &tmK, 0, y, z, bar, policy);
-          tma_load_3d(kdst + Cfg::kTileBytes, &tmV, 0, y, z, bar, policy);
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (aborted) {
-        volatile int never = 0;
-        for (int s = 0; s < STAGES; ++s)
-          if (issued & (1u << s)) mbar_wait_bounded(full0 + 8 * s, (issued_parity >> s) & 1u, &never);
-      }
-    }
+    if (lane == 0)
+      produce<Cfg::kTile, STAGES, Cfg::kStageBytes, 1, D, Cfg::kTileBytes, G, D * 4>(
+          &tmK, &tmV, p, sched, ring, smem_u32(qslots), full0, empty0, abort_flag);
     return;
   }
 
   // ------------------------------------------------------------------ consumers
-  const bool single = (p.num_splits == 1);
   int stage = 0;
   uint32_t phase = 0;
 
-  for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
-    const Item it = decode_item<Cfg::kTile>(p, i, nullptr, false);
-    if (it.tiles == 0 && !single) continue;
+  for (int i = blockIdx.x; i < sched.total; i += gridDim.x) {
+    const Item it = schedule_item<Cfg::kTile>(p, sched, i);
 
     const int head_base = it.hc * G;  // group-local index of this item's first head
-    // q pre-multiplied by scale * log2(e): scores come out in the log2 domain.
+    // q (pre-multiplied by scale * log2(e) once loaded, so scores come out in
+    // the log2 domain) arrives with the item's first stage.
     float qv[G][EPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const int hl = head_base + g;
-      if (hl < p.group) {
-        const float* qrow = static_cast<const float*>(p.q) +
-                            (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + hl) * D;
-        float tmp[EPL];
-        load_lane<EPL>(tmp, qrow + lane * EPL);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) qv[g][e] = tmp[e] * p.scale_log2;
-      } else {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) qv[g][e] = 0.f;
-      }
-    }
 
     float m_run[G], l_run[G], acc[G][EPL];
 #pragma unroll
@@ -173,6 +131,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       const float* ks = reinterpret_cast<const float*>(smem + size_t(stage) * Cfg::kStageBytes);
       const float* vs = ks + Cfg::kTile * D;
+      if (t == 0) {
+        const float* qs = reinterpret_cast<const float*>(qslots + size_t(stage) * Cfg::kQBytes);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float tmp[EPL];
+          load_lane<EPL>(tmp, qs + g * D + lane * EPL);
+          const bool ok = head_base + g < p.group;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) qv[g][e] = ok ? tmp[e] * p.scale_log2 : 0.f;
+        }
+      }
       const int valid = min(Cfg::kTile, it.row_end - (it.row_begin + t * Cfg::kTile));
       const int row0 = warp * RPW;
       const int nrows = min(RPW, valid - row0);  // may be <= 0
@@ -260,35 +229,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
       for (int e = 0; e < EPL; ++e) epi_acc[(warp * G + g) * D + lane * EPL + e] = acc[g][e];
     named_bar_sync(1, Cfg::kConsumerThreads);
-
-    if (!*abort_flag) {
-      for (int idx = threadIdx.x; idx < G * D; idx += Cfg::kConsumerThreads) {
-        const int g = idx / D;
-        const int d = idx % D;
-        const int hl = head_base + g;
-        if (hl >= p.group) continue;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, epi_m[w * G + g]);
-        float L = 0.f, sum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < W; ++w) {
-            const float f = ex2(epi_m[w * G + g] - M);
-            L += f * epi_l[w * G + g];
-            sum += f * epi_acc[(w * G + g) * D + d];
-          }
-        }
-        const float o = L > 0.f ? sum / L : 0.f;
-        const size_t bh = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + hl;
-        if (single) {
-          p.out[bh * D + d] = o;
-        } else {
-          p.o_part[(bh * p.num_splits + it.split) * D + d] = o;
-          if (d == 0) p.lse_part[bh * p.num_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
-        }
-      }
-    }
+    finish_item<D, 1, W, G, D>(p, it, epi_acc, epi_m, epi_l, threadIdx.x,
+                               Cfg::kConsumerThreads, abort_flag);
   }
 }
 

@@ -23,10 +23,11 @@
  *   including NaN.  A sequence with seq_lens[b] == 0 yields out = 0.
  *
  * The softmax is evaluated as a split-KV flash decode: the rows of each
- * (b, kv head) are cut into num_splits ranges of `chunk` rows, each range
- * produces a normalised partial output and its log-sum-exp, and a combine
- * step merges them.  The result equals the definition above up to float
- * rounding (fp32 accumulation throughout).
+ * sequence are cut into ranges of `chunk` rows, each (sequence, kv head,
+ * range) produces a normalised partial output and its log-sum-exp, and a
+ * combine kernel merges the ranges of every sequence that has more than one.
+ * The result equals the definition above up to float rounding (fp32
+ * accumulation).
  */
 #ifndef DECODE_ATTN_H_
 #define DECODE_ATTN_H_
@@ -77,19 +78,23 @@ typedef enum {
  */
 
 /*
- * Number of splits per (b, kv head) that decode_attn_ex will use for a
- * request: `num_splits` itself when > 0 (clamped so that every split holds
- * at least one tile of rows), else the library's choice for the current
- * device.  Returns a value >= 1, or a negative da_status.
+ * Upper bound on the splits per sequence that decode_attn_ex may use for a
+ * request (the workspace is sized for it).  With num_splits > 0 the split
+ * length is the whole number of pipeline stages closest to n_max / num_splits,
+ * so the bound is close to num_splits; with num_splits == 0 the kernels pick
+ * the split length on the device from the actual seq_lens, never shorter than
+ * this bound implies.  Returns a value >= 1, or a negative da_status.
  */
 DA_API int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
                                       int dtype, int num_splits);
 
 /*
- * Bytes of device workspace decode_attn_ex needs for this request (the
- * per-split partial outputs and log-sum-exps, float32).  0 when the request
- * resolves to a single split.  Returns 0 and sets *status (when non-NULL)
- * to a negative da_status if the arguments are invalid.
+ * Bytes of device workspace decode_attn_ex needs for this request: a 256-byte
+ * header and the per-split partial outputs and log-sum-exps (float32) of at
+ * most 1024 sequences (larger batches run as several launches that reuse
+ * it, one after the other on the stream).  0 when the request can only use
+ * one split.  Returns 0 and sets *status (when non-NULL) to a
+ * negative da_status if the arguments are invalid.
  */
 DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
                                           int dtype, int num_splits, int* status);
@@ -104,12 +109,15 @@ DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int
  *   workspace    : device memory of at least
  *                  decode_attn_workspace_bytes(...) bytes, 16-byte aligned;
  *                  may be NULL when that is 0.  Its contents need no
- *                  initialisation and are scratch after the call.
+ *                  initialisation and are scratch after the call.  Calls
+ *                  whose kernels may overlap on the GPU need separate
+ *                  workspaces.
  *   dev_error    : nullable device int32; kernels OR DA_DEVERR_* bits into it
  *                  (it is never cleared by the library).
  *   stream       : CUDA stream for every launch.
- * Launches one split kernel, plus one combine kernel when more than one
- * split is used.
+ * Launches, per slice of at most 1024 sequences, one split kernel and, when
+ * more than one split may be used, one combine kernel (programmatic
+ * dependent launch: it starts while the split kernel drains).
  */
 DA_API int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens,
                           float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,

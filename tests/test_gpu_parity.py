@@ -288,3 +288,15 @@ def test_mha_fp32_workload_sixteen_steps(o):
             torch.cuda.synchronize()
             check_against_oracle(o, q, K, V, lens + t + 1, w.scale, out.cpu(), TOL[w.dtype])
     assert torch.equal(Kd.cpu()[:, :, w.n:w.n + w.steps], K[:, :, w.n:w.n + w.steps])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_batch_larger_than_one_launch_slice(o, dtype):
+    """More than 1024 sequences run as several launches sharing one workspace."""
+    B = 1100
+    rng = np.random.default_rng(4)
+    lens = [int(x) for x in rng.integers(0, 70, B)]
+    q, K, V, lens_t, scale = make_case(B, 4, 2, 64, 70, lens, dtype, seed=5)
+    for splits in (0, 1, 3):
+        out = gpu_decode(q, K, V, lens_t, num_splits=splits)
+        check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])

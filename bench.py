@@ -1,7 +1,9 @@
 """Benchmark: decode-attention tokens/s and achieved HBM GB/s on one GB300.
 
-A step is one pass of the whole hot path over one batch: kv_append of the new
-K/V row of every (sequence, kv head), then decode_attn over the cache.  The
+A step is one pass of the whole hot path over one batch: the new K/V row of
+every (sequence, kv head) is appended and the decode runs over the grown cache,
+in one fused launch (``decode_attn_append``; ``--separate-append`` times
+``kv_append`` followed by ``decode_attn`` instead).  The
 step cycles through 16 consecutive positions (context n+1 ... n+16, as in
 the MHA fp32 workload's 16 append+decode steps), so the context length is the
 same however many steps run.  Inputs are seeded synthetic tensors resident in
@@ -279,11 +281,21 @@ def run_ours(args, w, world, rank, local):
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    fused = not args.separate_append
+
+    def step(i, qq=None, kn=None, vn=None):
+        """One pass of the hot path: append row pos of every kv head, decode over pos+1."""
         K, V = caches[i % n_rot]
         c = i % CYCLE
-        api.kv_append(k_new[c], v_new[c], K, V, pos_t[c])
-        api.decode_attn(q, K, V, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+        qq = q if qq is None else qq
+        kn = k_new[c] if kn is None else kn
+        vn = v_new[c] if vn is None else vn
+        if fused:
+            api.decode_attn_append(qq, kn, vn, K, V, pos_t[c], out=out, num_splits=w.num_splits,
+                                   workspace=ws)
+        else:
+            api.kv_append(kn, vn, K, V, pos_t[c])
+            api.decode_attn(qq, K, V, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
 
     for i in range(args.warmup):
         step(i)
@@ -294,7 +306,6 @@ def run_ours(args, w, world, rank, local):
         sampler.start()
         time.sleep(0.3)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     ev_start = torch.cuda.Event(enable_timing=True)
     ev_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -302,15 +313,12 @@ def run_ours(args, w, world, rank, local):
     launches0 = api.launch_count()
     if sampler:
         sampler.mark(True)
+    # Keep the GPU busy (outside the timed region) while the host queues the
+    # first steps, so that host launch latency does not leak into the timing.
+    torch.cuda._sleep(int(5e7))
     ev_start.record(stream)
     for i in range(K):
-        Kc, Vc = caches[i % n_rot]
-        c = i % CYCLE
-        ev[i][0].record(stream)
-        api.kv_append(k_new[c], v_new[c], Kc, Vc, pos_t[c])
-        ev[i][1].record(stream)
-        api.decode_attn(q, Kc, Vc, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
-        ev[i][2].record(stream)
+        step(i)
     ev_end.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -319,8 +327,6 @@ def run_ours(args, w, world, rank, local):
     launches = api.launch_count() - launches0
     total_ms = ev_start.elapsed_time(ev_end)
     total_ms = max_over_ranks(total_ms, world)
-    append_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     clocks = sampler.stop() if sampler else None
 
     # ---- end to end: pinned host inputs in, result out, every step
@@ -337,9 +343,7 @@ def run_ours(args, w, world, rank, local):
         q_d.copy_(q_h, non_blocking=True)
         kn_d.copy_(kn_h[c], non_blocking=True)
         vn_d.copy_(vn_h[c], non_blocking=True)
-        Kc, Vc = caches[i % n_rot]
-        api.kv_append(kn_d, vn_d, Kc, Vc, pos_t[c])
-        api.decode_attn(q_d, Kc, Vc, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+        step(i, q_d, kn_d, vn_d)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
     barrier(world)
@@ -349,9 +353,7 @@ def run_ours(args, w, world, rank, local):
         q_d.copy_(q_h, non_blocking=True)
         kn_d.copy_(kn_h[c], non_blocking=True)
         vn_d.copy_(vn_h[c], non_blocking=True)
-        Kc, Vc = caches[i % n_rot]
-        api.kv_append(kn_d, vn_d, Kc, Vc, pos_t[c])
-        api.decode_attn(q_d, Kc, Vc, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
+        step(i, q_d, kn_d, vn_d)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
@@ -364,12 +366,15 @@ def run_ours(args, w, world, rank, local):
     mean_lens = [int(n) + (CYCLE + 1) / 2 for n in lens0.tolist()]
     dec_bytes = accounting.decode_bytes(mean_lens, w.h_q, w.h_kv, w.d_k, w.d_v, es)
     app_bytes = accounting.append_bytes(w.B, w.h_kv, w.d_k, w.d_v, es)
+    # the fused call reads the new row once (from k_new/v_new) and writes it once
+    call_bytes = dec_bytes + app_bytes // 2 if fused else dec_bytes
     ms_per_step = total_ms / K
     tokens_per_s = world * w.B / (ms_per_step / 1e3)
     peak, peak_kind = peaks()
-    achieved = dec_bytes / (decode_ms / 1e3) / 1e9
+    step_bytes = call_bytes if fused else dec_bytes + app_bytes
+    achieved = step_bytes / (ms_per_step / 1e3) / 1e9
     traffic = recorded_traffic(w.name)
-    bytes_str = f"{dec_bytes / 1e6:.1f} MB per decode launch"
+    bytes_str = f"{step_bytes / 1e6:.1f} MB per step"
     if w.B * w.h_kv * w.n * (w.d_k + w.d_v) * es < L2_BYTES:
         bytes_str += " (L2-resident)"
 
@@ -380,14 +385,20 @@ def run_ours(args, w, world, rank, local):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.dtype == torch.float32 else "bf16",
         "data": "synthetic", "config": workload_config(wb, n_rot, kv_touch),
-        "hbm_gbs": (dec_bytes + app_bytes) / (ms_per_step / 1e3) / 1e9,
-        "hbm_frac_of_8tbs": (dec_bytes + app_bytes) / (ms_per_step / 1e3) / 8e12,
-        "decode_ms": decode_ms, "append_ms": append_ms, "max_splits": splits,
-        "roofline": {"bound": "hbm", "kernel": "decode_attn (split kernel"
-                     + (" + LSE combine)" if splits > 1 else ")"),
+        "hbm_gbs": achieved,
+        "hbm_frac_of_8tbs": achieved / 8000.0,
+        "step": "decode_attn_append (fused append + decode)" if fused
+        else "kv_append then decode_attn",
+        "max_splits": splits,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("split_decode kernel with fused append" if fused
+                                else "kv_append + split_decode kernels")
+                     + (" (+ PDL LSE combine)" if splits > 1 else ""),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": traffic, "algorithmic_bytes": dec_bytes, "per": bytes_str},
+                     "timing": "CUDA events around the K timed steps on the launching stream; "
+                               "one kernel per step (two when splits are merged)",
+                     "traffic": traffic, "algorithmic_bytes": step_bytes, "per": bytes_str},
         "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
                          "sample": cpu_sample},
         "e2e": {"value": world * w.B * e2e_steps / e2e_s, "unit": "tokens/s",
@@ -407,10 +418,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mha_fp32", choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--separate-append", action="store_true",
+                    help="run kv_append and decode_attn as two launches instead of the fused call")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="override the workload's splits per sequence (0 = library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = W.WORKLOADS[args.workload]
+    if args.splits is not None:
+        import dataclasses
+        w = dataclasses.replace(w, num_splits=args.splits)
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), rank)

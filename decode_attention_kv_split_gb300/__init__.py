@@ -9,6 +9,8 @@ from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
 from .api import (  # noqa: F401
     DecodeAttnError,
     decode_attn,
+    decode_attn_append,
+    decode_attn_noalloc,
     decode_attn_owned,
     kv_append,
     launch_count,

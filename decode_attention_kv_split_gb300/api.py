@@ -39,6 +39,8 @@ SIGNATURES = {
     "decode_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "decode_attn_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
     "decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "decode_attn_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                                _P, _SZ, _P, _P]),
     "decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]),
     "kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "decode_attn_status_string": (ctypes.c_char_p, [_I]),
@@ -89,6 +91,24 @@ def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+class _on_device:
+    """Make t's device current for the call (a no-op when it already is)."""
+
+    def __init__(self, t: torch.Tensor):
+        self.idx = t.device.index
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if self.idx is not None and cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+
+
 def _cache_dims(q, K, V, seq_lens):
     if q.dim() != 3 or K.dim() != 4 or V.dim() != 4:
         raise ValueError("expected q [B, h_q, d_k], K [B, h_kv, n_max, d_k], V [B, h_kv, n_max, d_v]")
@@ -115,11 +135,19 @@ def resolve_splits(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_splits
     return r
 
 
+_ws_bytes_cache: dict = {}
+
+
 def workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_splits: int = 0) -> int:
+    key = (torch.cuda.current_device(), B, h_q, h_kv, d_k, d_v, n_max, dtype, num_splits)
+    hit = _ws_bytes_cache.get(key)
+    if hit is not None:
+        return hit
     st = ctypes.c_int(0)
     n = load().decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, _DTYPES[dtype], num_splits,
                                            ctypes.byref(st))
     _check(st.value, "decode_attn_workspace_bytes")
+    _ws_bytes_cache[key] = int(n)
     return int(n)
 
 
@@ -156,7 +184,7 @@ def decode_attn(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, seq_lens: tor
         raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
     dt = _DTYPES[q.dtype]
     lib = load()
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, q.dtype, num_splits)
         if workspace is None:
             workspace = _workspace(q.device, need)
@@ -168,6 +196,43 @@ def decode_attn(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, seq_lens: tor
     return out
 
 
+def decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, K: torch.Tensor,
+                       V: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor | None = None,
+                       seq_lens_out: torch.Tensor | None = None, scale: float | None = None,
+                       num_splits: int = 0, workspace: torch.Tensor | None = None,
+                       dev_error: torch.Tensor | None = None,
+                       stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Append row seq_lens[b] of every kv head and decode over seq_lens[b] + 1 rows,
+    in one launch (calls ``decode_attn_append``); returns ``out``."""
+    B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
+    if k_new.shape != (B, h_kv, d_k) or v_new.shape != (B, h_kv, d_v):
+        raise ValueError("k_new/v_new must be [B, h_kv, d]")
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != K.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of the cache dtype")
+    if seq_lens_out is not None and (seq_lens_out.shape != (B,) or seq_lens_out.dtype != torch.int32):
+        raise ValueError("seq_lens_out must be an int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    if out is None:
+        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
+    elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
+    lib = load()
+    with _on_device(q):
+        need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, q.dtype, num_splits)
+        if workspace is None:
+            workspace = _workspace(q.device, need)
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.decode_attn_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V),
+                                    _ptr(seq_lens), _ptr(seq_lens_out), _ptr(out), B, h_q, h_kv,
+                                    d_k, d_v, n_max, float(scale), _DTYPES[q.dtype],
+                                    int(num_splits), _ptr(workspace), nbytes, _ptr(dev_error),
+                                    _stream(q, stream))
+    _check(st, "decode_attn_append")
+    return out
+
+
 def decode_attn_owned(q, K, V, seq_lens, out=None, scale=None, stream=None) -> torch.Tensor:
     """Decode attention through ``decode_attn`` (library-owned workspace)."""
     B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
@@ -175,7 +240,7 @@ def decode_attn_owned(q, K, V, seq_lens, out=None, scale=None, stream=None) -> t
         scale = 1.0 / math.sqrt(d_k)
     if out is None:
         out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         st = load().decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q, h_kv,
                                 d_k, d_v, n_max, float(scale), _DTYPES[q.dtype], _stream(q, stream))
     _check(st, "decode_attn")
@@ -195,7 +260,7 @@ def decode_attn_noalloc(q, K, V, seq_lens, out=None, scale=None, num_splits: int
         out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
     elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         st = load().decode_attn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q,
                                         h_kv, d_k, d_v, n_max, float(scale), _DTYPES[q.dtype],
                                         int(num_splits), _ptr(dev_error), _stream(q, stream))
@@ -220,7 +285,7 @@ def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, K: torch.Tensor, V: torc
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if not (k_new.dtype == v_new.dtype == K.dtype == V.dtype) or K.dtype not in _DTYPES:
         raise ValueError("k_new, v_new, K, V must share dtype float32 or bfloat16")
-    with torch.cuda.device(K.device):
+    with _on_device(K):
         st = load().kv_append(_ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V), _ptr(pos), B, h_kv, d_k,
                               d_v, n_max, _DTYPES[K.dtype], _ptr(dev_error), _stream(K, stream))
     _check(st, "kv_append")

@@ -81,10 +81,45 @@ int get_encoder(EncodeTiledFn* fn) {
   return DA_OK;
 }
 
+// Recently encoded descriptors: decode steps reuse the same caches, and an
+// encode costs more host time than the rest of a call.
+struct MapCacheEntry {
+  const void* base;
+  int dtype, d, n_max, heads, rows, cols, swz;
+  CUtensorMap map;
+};
+constexpr int kMapCacheSize = 32;
+MapCacheEntry g_map_cache[kMapCacheSize];
+int g_map_cache_next = 0;
+std::mutex g_map_mu;
+
+int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int d, int n_max,
+                              int heads, const KernelShape& ks);
+
 // A [rows_total = B*h_kv heads][n_max][d] cache viewed as a 3-D tensor
 // (innermost first): x = column, y = row inside a head, z = b*h_kv + head.
 int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int d, int n_max, int heads,
                      const KernelShape& ks) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (int i = 0; i < kMapCacheSize; ++i) {
+    const MapCacheEntry& e = g_map_cache[i];
+    if (e.base == base && e.dtype == dtype && e.d == d && e.n_max == n_max && e.heads == heads &&
+        e.rows == ks.tile_rows && e.cols == ks.box_cols && e.swz == ks.swizzle128) {
+      *map = e.map;
+      return DA_OK;
+    }
+  }
+  const int st = encode_cache_map_uncached(map, base, dtype, d, n_max, heads, ks);
+  if (st == DA_OK) {
+    MapCacheEntry& e = g_map_cache[g_map_cache_next];
+    g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
+    e = MapCacheEntry{base, dtype, d, n_max, heads, ks.tile_rows, ks.box_cols, ks.swizzle128, *map};
+  }
+  return st;
+}
+
+int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int d, int n_max,
+                              int heads, const KernelShape& ks) {
   EncodeTiledFn fn;
   int st = get_encoder(&fn);
   if (st != DA_OK) return st;
@@ -131,6 +166,31 @@ struct Plan {
   int batch_per_launch;
 };
 
+// The device-side cost model (choose_chunk) evaluated with every sequence at
+// n_max: if even full-length sequences are best served by one split, shorter
+// ones are too, and the launch needs neither partials nor a combine.
+bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, int sms) {
+  const long long grid = sms;  // the device model uses the whole persistent grid
+  const double share = double(n_max) * double(units) / double(grid);
+  double best_t = 1e300;
+  long long best_c = chunk_min;
+  for (int k = 0; k < 31; ++k) {
+    const long long c = (long long)chunk_min << k;
+    const long long per_seq_items = (n_max + c - 1) / c;
+    const double items = double(per_seq_items) * double(units);
+    const double rounds = ceil(items / double(grid));
+    const double ceff = double(c < n_max ? c : n_max);
+    double t = fmax(share, rounds * ceff / 1.6) + rounds * tile;
+    if (c < n_max) t += 2.0 * tile;
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best_c = c;
+    }
+    if (c >= n_max) break;
+  }
+  return best_c >= n_max;
+}
+
 // Splits per sequence requested by the caller -> a split length that is a
 // whole number of pipeline stages, as close as possible to n_max / S.  When
 // the library chooses, the device picks the length from the actual sequence
@@ -157,6 +217,10 @@ int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype, int request
     const long long per = (n_max + cap - 1) / cap;
     pl->chunk_fixed = 0;
     pl->chunk_min = int((per + tile - 1) / tile * tile);
+    if (single_split_suffices(units, n_max, pl->chunk_min, int(tile), sms)) {
+      pl->chunk_fixed = int(max_tiles * tile);  // one split: no partials, no combine
+      pl->chunk_min = pl->chunk_fixed;
+    }
   }
   const long long splits = (n_max + pl->chunk_min - 1) / pl->chunk_min;
   if (splits >= (1 << 20)) return DA_ERR_SHAPE;
@@ -190,6 +254,75 @@ struct OwnedWorkspace {
 };
 OwnedWorkspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
+
+int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_lens,
+                      float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                      float scale, int dtype, int num_splits, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream,
+                      const void* k_new, const void* v_new, int32_t* seq_lens_out) {
+  if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
+  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype);
+  if (st != DA_OK) return st;
+  if (!isfinite(scale)) return DA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return DA_ERR_ALIGN;
+  int dev, sms;
+  if ((st = current_device(&dev, &sms)) != DA_OK) return st;
+  Plan pl;
+  if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
+  const WorkspaceLayout wl = workspace_layout(pl, h_q, d_k);
+  if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return DA_ERR_WORKSPACE;
+
+  CUtensorMap tk, tv;
+  if ((st = encode_cache_map(&tk, K, dtype, d_k, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
+  if ((st = encode_cache_map(&tv, V, dtype, d_v, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
+
+  const int es = dtype == DA_BF16 ? 2 : 4;
+  char* ws = static_cast<char*>(workspace);
+  for (int b0 = 0; b0 < B; b0 += pl.batch_per_launch) {
+    const int bn = (B - b0) < pl.batch_per_launch ? (B - b0) : pl.batch_per_launch;
+    SplitParams p;
+    p.q = static_cast<const char*>(q) + size_t(b0) * h_q * d_k * es;
+    p.seq_lens = seq_lens + b0;
+    p.out = out + size_t(b0) * h_q * d_v;
+    p.o_part = wl.total ? reinterpret_cast<float*>(ws + wl.o_part) : nullptr;
+    p.lse_part = wl.total ? reinterpret_cast<float*>(ws + wl.lse_part) : nullptr;
+    p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
+    p.dev_error = dev_error;
+    p.append = k_new != nullptr;
+    p.k_new = k_new ? static_cast<const char*>(k_new) + size_t(b0) * h_kv * d_k * es : nullptr;
+    p.v_new = v_new ? static_cast<const char*>(v_new) + size_t(b0) * h_kv * d_v * es : nullptr;
+    p.k_cache = const_cast<void*>(K);
+    p.v_cache = const_cast<void*>(V);
+    p.seq_lens_out = seq_lens_out ? seq_lens_out + b0 : nullptr;
+    p.B = bn;
+    p.h_q = h_q;
+    p.h_kv = h_kv;
+    p.group = h_q / h_kv;
+    p.b_offset = b0;
+    p.n_max = n_max;
+    p.head_chunks = pl.head_chunks;
+    p.chunk_fixed = pl.chunk_fixed;
+    p.chunk_min = pl.chunk_min;
+    p.max_splits = pl.max_splits;
+    p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
+    const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
+    const int grid = int(items < sms ? items : sms);
+    cudaError_t err = dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
+                                       : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
+    if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
+    g_launches.fetch_add(1);
+    if (wl.total) {
+      err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.append, p.out, bn,
+                               h_q, d_v, pl.max_splits, n_max, stream);
+      if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
+      g_launches.fetch_add(1);
+    }
+  }
+  return DA_OK;
+}
+
 
 }  // namespace
 
@@ -240,61 +373,22 @@ int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* s
                    int B, int h_q, int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
                    int num_splits, void* workspace, size_t workspace_bytes, int32_t* dev_error,
                    cudaStream_t stream) {
-  if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
-  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype);
-  if (st != DA_OK) return st;
-  if (!isfinite(scale)) return DA_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
-      (workspace && !aligned16(workspace)))
-    return DA_ERR_ALIGN;
-  int dev, sms;
-  if ((st = current_device(&dev, &sms)) != DA_OK) return st;
-  Plan pl;
-  if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
-  const WorkspaceLayout wl = workspace_layout(pl, h_q, d_k);
-  if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return DA_ERR_WORKSPACE;
+  return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
+                    num_splits, workspace, workspace_bytes, dev_error, stream, nullptr, nullptr,
+                    nullptr);
+}
 
-  CUtensorMap tk, tv;
-  if ((st = encode_cache_map(&tk, K, dtype, d_k, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
-  if ((st = encode_cache_map(&tv, V, dtype, d_v, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
-
-  const int es = dtype == DA_BF16 ? 2 : 4;
-  char* ws = static_cast<char*>(workspace);
-  for (int b0 = 0; b0 < B; b0 += pl.batch_per_launch) {
-    const int bn = (B - b0) < pl.batch_per_launch ? (B - b0) : pl.batch_per_launch;
-    SplitParams p;
-    p.q = static_cast<const char*>(q) + size_t(b0) * h_q * d_k * es;
-    p.seq_lens = seq_lens + b0;
-    p.out = out + size_t(b0) * h_q * d_v;
-    p.o_part = wl.total ? reinterpret_cast<float*>(ws + wl.o_part) : nullptr;
-    p.lse_part = wl.total ? reinterpret_cast<float*>(ws + wl.lse_part) : nullptr;
-    p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
-    p.dev_error = dev_error;
-    p.B = bn;
-    p.h_q = h_q;
-    p.h_kv = h_kv;
-    p.group = h_q / h_kv;
-    p.b_offset = b0;
-    p.n_max = n_max;
-    p.head_chunks = pl.head_chunks;
-    p.chunk_fixed = pl.chunk_fixed;
-    p.chunk_min = pl.chunk_min;
-    p.max_splits = pl.max_splits;
-    p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
-    const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
-    const int grid = int(items < sms ? items : sms);
-    cudaError_t err = dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
-                                       : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
-    if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
-    g_launches.fetch_add(1);
-    if (wl.total) {
-      err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.out, bn, h_q, d_v,
-                               pl.max_splits, n_max, stream);
-      if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
-      g_launches.fetch_add(1);
-    }
-  }
-  return DA_OK;
+int decode_attn_append(const void* q, const void* k_new, const void* v_new, void* K, void* V,
+                       const int32_t* seq_lens, int32_t* seq_lens_out, float* out, int B, int h_q,
+                       int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
+                       int num_splits, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_error, cudaStream_t stream) {
+  if (!k_new || !v_new) return DA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return DA_ERR_ALIGN;
+  if (seq_lens_out && seq_lens_out == seq_lens) return DA_ERR_SHAPE;
+  return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
+                    num_splits, workspace, workspace_bytes, dev_error, stream, k_new, v_new,
+                    seq_lens_out);
 }
 
 int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens, float* out,

@@ -25,7 +25,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
     lse_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                        const int* __restrict__ chunk_in, const int32_t* __restrict__ seq_lens,
-                       float* __restrict__ out, int h_q, int max_splits, int n_max) {
+                       int append, float* __restrict__ out, int h_q, int max_splits, int n_max) {
   constexpr int EPL = D / 32;
   constexpr int kWarps = 8;
   __shared__ float red_m[kWarps];
@@ -39,7 +39,9 @@ __global__ void __launch_bounds__(256)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int n = __ldg(seq_lens + b);
+  const bool appended = append && n >= 0 && n < n_max;  // same rule as the split kernel
   n = n < 0 ? 0 : (n > n_max ? n_max : n);
+  if (appended) ++n;
   const int chunk = *reinterpret_cast<const volatile int*>(chunk_in);
   const int nv = n <= 0 ? 1 : (n + chunk - 1) / chunk;
   if (nv <= 1 || chunk <= 0) return;  // written by the split kernel
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, float* out, int B, int h_q, int d,
+                           const int32_t* seq_lens, int append, float* out, int B, int h_q, int d,
                            int max_splits, int n_max, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(B) * unsigned(h_q));
@@ -115,9 +117,9 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const int
   cfg.numAttrs = 1;
   if (d == 128)
     return cudaLaunchKernelEx(&cfg, lse_combine_kernel<128>, o_part, lse_part, chunk_in, seq_lens,
-                              out, h_q, max_splits, n_max);
+                              append, out, h_q, max_splits, n_max);
   return cudaLaunchKernelEx(&cfg, lse_combine_kernel<64>, o_part, lse_part, chunk_in, seq_lens,
-                            out, h_q, max_splits, n_max);
+                            append, out, h_q, max_splits, n_max);
 }
 
 }  // namespace da

@@ -29,6 +29,14 @@ struct SplitParams {
   float* lse_part;               // [B, h_q, max_splits]     log2-domain log-sum-exp
   int* chunk_out;                // workspace word receiving the split length used (nullable)
   int32_t* dev_error;            // nullable
+  // Fused append (append != 0): before decoding, row seq_lens[b] of every kv
+  // head of K/V receives k_new[b, h] / v_new[b, h] and takes part in the decode.
+  const void* k_new;             // [B, h_kv, d]
+  const void* v_new;             // [B, h_kv, d]
+  void* k_cache;                 // K base (all sequences; b_offset applies)
+  void* v_cache;                 // V base
+  int32_t* seq_lens_out;         // nullable: receives the lengths after the append
+  int append;
   int B, h_q, h_kv, group;       // group = h_q / h_kv
   int b_offset;                  // first sequence of this launch inside the tensor maps
   int n_max;
@@ -135,6 +143,12 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Named barrier over a subset of warps (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -208,7 +222,7 @@ cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, float* out, int B, int h_q, int d,
+                           const int32_t* seq_lens, int append, float* out, int B, int h_q, int d,
                            int max_splits, int n_max, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void* V,
                              const int32_t* pos, int B, int h_kv, int row_bytes_k,
@@ -226,15 +240,19 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void
 // ---------------------------------------------------------------------------
 struct Schedule {
   int* first;       // [B + 1] first item of sequence b (shared memory)
-  int* lens;        // [B] clamped lengths (shared memory)
+  int* lens;        // [B] rows to decode; bit 31 set when row (len - 1) is appended now
   int chunk;
   int total;
 };
+
+constexpr int kAppendFlag = int(0x80000000u);
+__device__ __forceinline__ int len_of(int v) { return v & 0x7fffffff; }
 
 struct Item {
   int b, kvh, hc, split, nv;
   int row_begin, row_end;  // rows [row_begin, row_end) of head (b, kvh)
   int tiles;
+  int new_row;             // row appended by this call (-1: none); the unit's last row
 };
 
 template <int TILE>
@@ -254,7 +272,8 @@ __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedu
   it.split = r - unit * it.nv;
   it.kvh = unit / p.head_chunks;
   it.hc = unit - it.kvh * p.head_chunks;
-  const int n = s.lens[lo];
+  const int n = len_of(s.lens[lo]);
+  it.new_row = (s.lens[lo] & kAppendFlag) ? n - 1 : -1;
   it.row_begin = it.split * s.chunk;
   const int end = it.row_begin + s.chunk;
   it.row_end = end < n ? end : n;
@@ -282,7 +301,7 @@ __device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* len
     long long rows = 0;
     int nmax = 0;
     for (int b = lane; b < p.B; b += 32) {
-      const int n = lens[b];
+      const int n = len_of(lens[b]);
       rows += n;
       nmax = n > nmax ? n : nmax;
       const unsigned u = n <= 0 ? 1u : unsigned((n + p.chunk_min - 1) / p.chunk_min);
@@ -350,15 +369,24 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* fi
                                                    int* red) {
   const int tid = threadIdx.x;
   bool bad = false;
+  bool bad_pos = false;
   for (int b = tid; b < p.B; b += blockDim.x) {
     int n = __ldg(p.seq_lens + b);
+    bool app = false;
+    if (p.append) {
+      app = n >= 0 && n < p.n_max;  // room for the new row
+      bad_pos |= !app;
+    }
     if (n < 0 || n > p.n_max) {
       bad = true;
       n = n < 0 ? 0 : p.n_max;
     }
-    lens[b] = n;
+    if (app) ++n;
+    lens[b] = app ? (n | kAppendFlag) : n;
+    if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n;
   }
   if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
+  if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
   __syncthreads();
   Schedule s;
   s.first = first;
@@ -372,7 +400,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* fi
       const int b = base + tid;
       int c = 0;
       if (b < p.B) {
-        const int n = lens[b];
+        const int n = len_of(lens[b]);
         c = per_seq * (n <= 0 ? 1 : (n + s.chunk - 1) / s.chunk);
       }
       int x = c;
@@ -440,6 +468,24 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
   }
 }
 
+// Fused append: copy the new K and V rows (shared-memory slot, K row then V
+// row, ROW_BYTES each) into row `row` of kv head (b_offset + b, kvh) of the
+// caches.  One warp; an exact copy of the bits.
+template <int ROW_BYTES>
+__device__ __forceinline__ void store_new_row(const SplitParams& p, const Item& it,
+                                              const uint8_t* slot, int lane) {
+  const size_t head = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
+  const size_t off = (head * size_t(p.n_max) + size_t(it.new_row)) * ROW_BYTES;
+  const uint4* ks = reinterpret_cast<const uint4*>(slot);
+  const uint4* vs = reinterpret_cast<const uint4*>(slot + ROW_BYTES);
+  uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + off);
+  uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(p.v_cache) + off);
+  for (int i = lane; i < ROW_BYTES / 16; i += 32) {
+    kd[i] = ks[i];
+    vd[i] = vs[i];
+  }
+}
+
 // Let a combine kernel launched with programmatic stream serialisation start
 // its launch while this grid is still running (it waits for our completion).
 __device__ __forceinline__ void allow_dependent_launch() {
@@ -458,12 +504,15 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
 // ---------------------------------------------------------------------------
 // The query rows of an item (its head chunk of one kv group, contiguous in
 // q) ride with the item's first stage into that stage's q slot.
+// With a fused append, the new K and V rows of the unit ride with the stage
+// that holds the unit's last row, into that stage's new-row slot
+// (2 * ROW_BYTES: the K row, then the V row).
 template <int TILE, int STAGES, int STAGE_BYTES, int NBOX, int BOX_COLS, int BOX_BYTES,
           int HEADS, int ROW_BYTES>
 __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMap* tmV,
                                         const SplitParams& p, const Schedule& s, uint32_t ring,
-                                        uint32_t qslots, uint32_t full0, uint32_t empty0,
-                                        volatile int* abort_flag) {
+                                        uint32_t qslots, uint32_t newslots, uint32_t full0,
+                                        uint32_t empty0, volatile int* abort_flag) {
   prefetch_tmap(tmK);
   prefetch_tmap(tmV);
   const uint64_t policy = l2_policy_evict_first();
@@ -482,16 +531,29 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
         break;
       }
       const uint32_t bar = full0 + 8 * stage;
+      const int y0 = it.row_begin + t * TILE;
+      const bool with_new = it.new_row >= y0 && it.new_row < y0 + TILE;
+      uint32_t extra = 0;
       if (t == 0) {
         const int h0 = it.hc * HEADS;
         const int nh = min(HEADS, p.group - h0);
-        const uint32_t qbytes = uint32_t(nh) * ROW_BYTES;
-        mbar_arrive_expect_tx(bar, STAGE_BYTES + qbytes);
+        extra += uint32_t(nh) * ROW_BYTES;
+      }
+      if (with_new) extra += 2 * ROW_BYTES;
+      mbar_arrive_expect_tx(bar, STAGE_BYTES + extra);
+      if (t == 0) {
+        const int h0 = it.hc * HEADS;
+        const int nh = min(HEADS, p.group - h0);
         const char* qsrc = static_cast<const char*>(p.q) +
                            (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * ROW_BYTES;
-        bulk_load(qslots + stage * (HEADS * ROW_BYTES), qsrc, qbytes, bar);
-      } else {
-        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        bulk_load(qslots + stage * (HEADS * ROW_BYTES), qsrc, uint32_t(nh) * ROW_BYTES, bar);
+      }
+      if (with_new) {
+        const size_t src = (size_t(it.b) * p.h_kv + it.kvh) * ROW_BYTES;
+        bulk_load(newslots + stage * (2 * ROW_BYTES), static_cast<const char*>(p.k_new) + src,
+                  ROW_BYTES, bar);
+        bulk_load(newslots + stage * (2 * ROW_BYTES) + ROW_BYTES,
+                  static_cast<const char*>(p.v_new) + src, ROW_BYTES, bar);
       }
       const uint32_t kdst = ring + stage * STAGE_BYTES;
       const int y = it.row_begin + t * TILE;

@@ -52,7 +52,8 @@ struct Bf16Cfg {
   // (rounded up to an even count of 4-byte words)
   static constexpr int kSchedWords = (2 * kMaxBatchPerLaunch + 1 + 48 + 1) & ~1;
   static constexpr int kQBytes = kHeadsPerCta * D * 2;  // q rows of one item, per stage
-  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes) +
+  static constexpr int kNewBytes = 2 * D * 2;              // appended K and V rows, per stage
+  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes + kNewBytes) +
                                        size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 +
                                        2 * STAGES * 8 + 16;
   static_assert(D == 64 || D == 128, "head dim");
@@ -81,7 +82,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* qslots = smem + size_t(STAGES) * Cfg::kStageBytes;
-  float* epi_acc = reinterpret_cast<float*>(qslots + size_t(STAGES) * Cfg::kQBytes);
+  uint8_t* newslots = qslots + size_t(STAGES) * Cfg::kQBytes;
+  float* epi_acc = reinterpret_cast<float*>(newslots + size_t(STAGES) * Cfg::kNewBytes);
   float* epi_m = epi_acc + Cfg::kEpiAccFloats;
   float* epi_l = epi_m + Cfg::HG * KW * kHPW;
   int* sched_first = reinterpret_cast<int*>(epi_l + Cfg::HG * KW * kHPW);
@@ -111,8 +113,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == Cfg::kConsumerWarps) {
     if (lane == 0)
       produce<Cfg::kTile, STAGES, Cfg::kStageBytes, Cfg::kHalves, 64, Cfg::kHalfBytes,
-              Cfg::kHeadsPerCta, D * 2>(&tmK, &tmV, p, sched, ring, smem_u32(qslots), full0,
-                                        empty0, abort_flag);
+              Cfg::kHeadsPerCta, D * 2>(&tmK, &tmV, p, sched, ring, smem_u32(qslots),
+                                        smem_u32(newslots), full0, empty0, abort_flag);
     return;
   }
 
@@ -155,8 +157,33 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       const uint32_t kbase = ring + stage * Cfg::kStageBytes;
       const uint32_t vbase = kbase + Cfg::kTileBytes;
-      const int valid = min(Cfg::kTile, it.row_end - (it.row_begin + t * Cfg::kTile));
+      const int tile_row0 = it.row_begin + t * Cfg::kTile;
+      const int valid = min(Cfg::kTile, it.row_end - tile_row0);
       const int key0 = kw * KBW * 16;  // first row of this warp inside the stage
+      // A row appended by this call replaces the stale cache row the tile load
+      // brought in.
+      const int new_local = (it.new_row >= tile_row0 && it.new_row < tile_row0 + Cfg::kTile)
+                                ? it.new_row - tile_row0
+                                : -1;
+      if (new_local >= 0) {  // the same for every consumer warp
+        if (warp == 0 && !*abort_flag) {
+          // Put the appended rows into the stage, in the tile's swizzled layout,
+          // and (once per kv head) into the caches.
+          const uint8_t* slot = newslots + size_t(stage) * Cfg::kNewBytes;
+          uint8_t* ktile = smem + size_t(stage) * Cfg::kStageBytes;
+          uint8_t* vtile = ktile + Cfg::kTileBytes;
+          for (int ch = lane; ch < D / 8; ch += 32) {
+            const int col = ch * 8;
+            *reinterpret_cast<uint4*>(ktile + swz<Cfg>(new_local, col)) =
+                *reinterpret_cast<const uint4*>(slot + col * 2);
+            *reinterpret_cast<uint4*>(vtile + swz<Cfg>(new_local, col)) =
+                *reinterpret_cast<const uint4*>(slot + D * 2 + col * 2);
+          }
+          if (it.hc == 0) store_new_row<D * 2>(p, it, slot, lane);
+          fence_proxy_async_smem();
+        }
+        named_bar_sync(2, Cfg::kConsumerThreads);
+      }
       if (t == 0) {
         const uint32_t* qs =
             reinterpret_cast<const uint32_t*>(qslots + size_t(stage) * Cfg::kQBytes);

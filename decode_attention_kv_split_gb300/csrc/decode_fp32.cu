@@ -36,7 +36,8 @@ struct F32Cfg {
   static constexpr int kEpiMLFloats = 2 * W * G;
   static constexpr int kSchedWords = (2 * kMaxBatchPerLaunch + 1 + 48 + 1) & ~1;
   static constexpr int kQBytes = G * D * 4;  // q rows of one item, per stage
-  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes) +
+  static constexpr int kNewBytes = 2 * D * 4;  // appended K and V rows, per stage
+  static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes + kNewBytes) +
                                        size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 +
                                        2 * STAGES * 8 + 16;
   static_assert((kEpiAccFloats + kEpiMLFloats) % 2 == 0, "mbarrier alignment");
@@ -67,7 +68,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* qslots = smem + size_t(STAGES) * Cfg::kStageBytes;
-  float* epi_acc = reinterpret_cast<float*>(qslots + size_t(STAGES) * Cfg::kQBytes);
+  uint8_t* newslots = qslots + size_t(STAGES) * Cfg::kQBytes;
+  float* epi_acc = reinterpret_cast<float*>(newslots + size_t(STAGES) * Cfg::kNewBytes);
   float* epi_m = epi_acc + Cfg::kEpiAccFloats;
   float* epi_l = epi_m + W * G;
   int* sched_first = reinterpret_cast<int*>(epi_l + W * G);
@@ -97,7 +99,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == W) {
     if (lane == 0)
       produce<Cfg::kTile, STAGES, Cfg::kStageBytes, 1, D, Cfg::kTileBytes, G, D * 4>(
-          &tmK, &tmV, p, sched, ring, smem_u32(qslots), full0, empty0, abort_flag);
+          &tmK, &tmV, p, sched, ring, smem_u32(qslots), smem_u32(newslots), full0, empty0,
+          abort_flag);
     return;
   }
 
@@ -142,9 +145,32 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           for (int e = 0; e < EPL; ++e) qv[g][e] = ok ? tmp[e] * p.scale_log2 : 0.f;
         }
       }
-      const int valid = min(Cfg::kTile, it.row_end - (it.row_begin + t * Cfg::kTile));
+      const int tile_row0 = it.row_begin + t * Cfg::kTile;
+      const int valid = min(Cfg::kTile, it.row_end - tile_row0);
       const int row0 = warp * RPW;
       const int nrows = min(RPW, valid - row0);  // may be <= 0
+      // A row appended by this call replaces the stale cache row the tile load
+      // brought in.
+      const int new_local = (it.new_row >= tile_row0 && it.new_row < tile_row0 + Cfg::kTile)
+                                ? it.new_row - tile_row0
+                                : -1;
+      if (new_local >= 0) {  // the same for every consumer warp
+        if (warp == 0 && !*abort_flag) {
+          // Put the appended rows into the stage and (once per kv head) into the caches.
+          const uint8_t* slot = newslots + size_t(stage) * Cfg::kNewBytes;
+          uint8_t* ktile = smem + size_t(stage) * Cfg::kStageBytes;
+          uint8_t* vtile = ktile + Cfg::kTileBytes;
+          for (int ch = lane; ch < D / 4; ch += 32) {
+            reinterpret_cast<uint4*>(ktile + size_t(new_local) * D * 4)[ch] =
+                reinterpret_cast<const uint4*>(slot)[ch];
+            reinterpret_cast<uint4*>(vtile + size_t(new_local) * D * 4)[ch] =
+                reinterpret_cast<const uint4*>(slot + D * 4)[ch];
+          }
+          if (it.hc == 0) store_new_row<D * 4>(p, it, slot, lane);
+          fence_proxy_async_smem();
+        }
+        named_bar_sync(2, Cfg::kConsumerThreads);
+      }
 
       if (!*abort_flag && nrows > 0) {
         // Step I: s[g][r] = (scale*log2e*q_g) . K_row, reduced across the warp.

@@ -125,6 +125,28 @@ DA_API int decode_attn_ex(const void* q, const void* K, const void* V, const int
                           size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream);
 
 /*
+ * One decode step with the KV-cache append fused in ("MoA-Structured Decode
+ * Attention", introduction item 3 followed by section 2): for every b with
+ * 0 <= seq_lens[b] < n_max, row seq_lens[b] of every kv head of K and V
+ * receives k_new[b, h, :] / v_new[b, h, :] (an exact copy of the bits, as
+ * kv_append does) and the decode runs over seq_lens[b] + 1 rows, the new row
+ * included, all in the same launch.  A sequence whose seq_lens[b] is outside
+ * [0, n_max) gets no new row (DA_DEVERR_POS) and is decoded over its clamped
+ * length.
+ *   k_new [B, h_kv, d_k], v_new [B, h_kv, d_v] : device, dtype, 16-byte aligned
+ *   seq_lens      : device int32 [B], the lengths before the append (read only)
+ *   seq_lens_out  : nullable device int32 [B]; receives the lengths after the
+ *                   append.  Must not be seq_lens itself.
+ *   other arguments, workspace and errors: as decode_attn_ex (the workspace
+ *   size is decode_attn_workspace_bytes of the same request).
+ */
+DA_API int decode_attn_append(const void* q, const void* k_new, const void* v_new, void* K, void* V,
+                              const int32_t* seq_lens, int32_t* seq_lens_out, float* out, int B,
+                              int h_q, int h_kv, int d_k, int d_v, int n_max, float scale,
+                              int dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_error, cudaStream_t stream);
+
+/*
  * Decode attention with a library-owned workspace: the same computation as
  * decode_attn_ex with num_splits = 0 (library's choice).  The workspace is
  * cached per device and grown with cudaMalloc when a request needs more (a

@@ -300,3 +300,74 @@ def test_batch_larger_than_one_launch_slice(o, dtype):
     for splits in (0, 1, 3):
         out = gpu_decode(q, K, V, lens_t, num_splits=splits)
         check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
+# ----------------------------------------------------------------- fused append + decode
+def _bits(t):
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).numpy()
+
+
+APPEND_CASES = [
+    # B, h_q, h_kv, d, n_max, lens before the append
+    (3, 8, 2, 128, 300, [0, 127, 299]),       # empty, a stage boundary, the last free row
+    (2, 32, 1, 128, 700, [699, 320]),         # MQA
+    (2, 64, 1, 64, 260, [128, 255]),          # two head chunks
+    (4, 4, 4, 64, 200, [63, 64, 65, 200]),    # last one has no room: no append, flagged
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("case", APPEND_CASES, ids=[f"case{i}" for i in range(len(APPEND_CASES))])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_fused_append_decode(o, dtype, case, splits):
+    B, h_q, h_kv, d, n_max, lens = case
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=B + h_q)
+    w = W.custom(B=B, h_q=h_q, h_kv=h_kv, d_k=d, n=max(lens), n_max=n_max, dtype=dtype)
+    kn, vn = W.new_rows(w, 3, seed=7)
+    dev = torch.device("cuda")
+    Kd, Vd = K.to(dev), V.to(dev)
+    err = torch.zeros((), dtype=torch.int32, device=dev)
+    lens_out = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    out = torch.full((B, h_q, d), float("nan"), device=dev)
+    api.decode_attn_append(q.to(dev), kn.to(dev), vn.to(dev), Kd, Vd, lens_t.to(dev), out=out,
+                           seq_lens_out=lens_out, num_splits=splits, dev_error=err)
+    torch.cuda.synchronize()
+    # oracle: append, then decode over the grown lengths
+    Kw, Vw = _bits(K).copy(), _bits(V).copy()
+    skipped = o.kv_append(_bits(kn).copy(), _bits(vn).copy(), Kw, Vw, lens_t.numpy())
+    grown = torch.tensor([n + 1 if n < n_max else n for n in lens], dtype=torch.int32)
+    assert np.array_equal(_bits(Kd.cpu()), Kw) and np.array_equal(_bits(Vd.cpu()), Vw)
+    assert torch.equal(lens_out.cpu(), grown)
+    assert bool(int(err.item()) & api.DEVERR_POS) == (skipped > 0)
+    K2 = torch.from_numpy(Kw).view(dtype)
+    V2 = torch.from_numpy(Vw).view(dtype)
+    check_against_oracle(o, q, K2, V2, grown, scale, out.cpu(), TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_fused_append_sixteen_steps(o, dtype):
+    """Sixteen fused steps, lengths ping-ponged through seq_lens_out, equal the
+    oracle's sixteen appends and decodes."""
+    B, h_q, h_kv, d, n0, steps = 2, 8, 4, 128, 250, 16
+    n_max = n0 + steps
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, [n0, n0 - 100], dtype, seed=11)
+    w = W.custom(B=B, h_q=h_q, h_kv=h_kv, d_k=d, n=n0, n_max=n_max, dtype=dtype)
+    dev = torch.device("cuda")
+    Kd, Vd, qd = K.to(dev), V.to(dev), q.to(dev)
+    la, lb = lens_t.to(dev), torch.empty(B, dtype=torch.int32, device=dev)
+    Kw, Vw = _bits(K).copy(), _bits(V).copy()
+    lens_np = lens_t.numpy().copy()
+    for t in range(steps):
+        kn, vn = W.new_rows(w, t, seed=13)
+        out = api.decode_attn_append(qd, kn.to(dev), vn.to(dev), Kd, Vd, la, seq_lens_out=lb,
+                                     num_splits=2)
+        o.kv_append(_bits(kn).copy(), _bits(vn).copy(), Kw, Vw, lens_np)
+        lens_np += 1
+        la, lb = lb, la
+        if t in (0, steps - 1):
+            torch.cuda.synchronize()
+            check_against_oracle(o, q, torch.from_numpy(Kw).view(dtype),
+                                 torch.from_numpy(Vw).view(dtype), torch.from_numpy(lens_np),
+                                 scale, out.cpu(), TOL[dtype])
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(Kd.cpu()), Kw) and np.array_equal(_bits(Vd.cpu()), Vw)

@@ -159,6 +159,7 @@ int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype
 
 struct Plan {
   KernelShape ks;
+  bool tc5;            // bf16, d = 128, group > 8: the tcgen05 kernel
   int head_chunks;
   int chunk_fixed;     // > 0: rows per split fixed by the caller's num_splits
   int chunk_min;       // else: the device picks chunk_min * 2^k
@@ -169,24 +170,34 @@ struct Plan {
 // The device-side cost model (choose_chunk) evaluated with every sequence at
 // n_max: if even full-length sequences are best served by one split, shorter
 // ones are too, and the launch needs neither partials nor a combine.
-bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, int sms) {
+bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, int sms,
+                           float cta_speed) {
   const long long grid = sms;  // the device model uses the whole persistent grid
   const double share = double(n_max) * double(units) / double(grid);
   double best_t = 1e300;
   long long best_c = chunk_min;
-  for (int k = 0; k < 31; ++k) {
-    const long long c = (long long)chunk_min << k;
+  for (int k = 0; k < 32; ++k) {
+    long long c;
+    if (k < 16) {
+      c = (long long)chunk_min << k;
+      if (k > 0 && ((long long)chunk_min << (k - 1)) >= n_max) continue;
+    } else {
+      long long pieces = (long long)(k - 15) * grid / units;
+      if (pieces < 1) pieces = 1;
+      c = (n_max + pieces - 1) / pieces;
+    }
+    c = (c + tile - 1) / tile * tile;
+    if (c < chunk_min) c = chunk_min;
     const long long per_seq_items = (n_max + c - 1) / c;
     const double items = double(per_seq_items) * double(units);
     const double rounds = ceil(items / double(grid));
     const double ceff = double(c < n_max ? c : n_max);
-    double t = fmax(share, rounds * ceff / 1.6) + rounds * tile;
+    double t = fmax(share, rounds * ceff / cta_speed) + rounds * tile;
     if (c < n_max) t += 2.0 * tile;
-    if (t < best_t * 0.999) {
+    if (t < best_t * 0.999 || (t <= best_t * 1.001 && c < best_c)) {
       best_t = t;
       best_c = c;
     }
-    if (c >= n_max) break;
   }
   return best_c >= n_max;
 }
@@ -199,7 +210,9 @@ bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, 
 int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype, int requested, int sms,
               Plan* pl) {
   const int group = h_q / h_kv;
-  pl->ks = dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group);
+  pl->tc5 = dtype == DA_BF16 && d == 128 && group > 8;
+  pl->ks = pl->tc5 ? da::tc5_shape(group)
+                   : (dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group));
   pl->head_chunks = (group + pl->ks.heads_per_cta - 1) / pl->ks.heads_per_cta;
   pl->batch_per_launch = B < da::kMaxBatchPerLaunch ? B : da::kMaxBatchPerLaunch;
   const long long tile = pl->ks.tile_rows;
@@ -217,7 +230,7 @@ int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype, int request
     const long long per = (n_max + cap - 1) / cap;
     pl->chunk_fixed = 0;
     pl->chunk_min = int((per + tile - 1) / tile * tile);
-    if (single_split_suffices(units, n_max, pl->chunk_min, int(tile), sms)) {
+    if (single_split_suffices(units, n_max, pl->chunk_min, int(tile), sms, pl->ks.cta_speed)) {
       pl->chunk_fixed = int(max_tiles * tile);  // one split: no partials, no combine
       pl->chunk_min = pl->chunk_fixed;
     }
@@ -306,11 +319,13 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.chunk_fixed = pl.chunk_fixed;
     p.chunk_min = pl.chunk_min;
     p.max_splits = pl.max_splits;
+    p.cta_speed = pl.ks.cta_speed;
     p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
     const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
     const int grid = int(items < sms ? items : sms);
-    cudaError_t err = dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
-                                       : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
+    cudaError_t err = pl.tc5 ? da::launch_split_tc5(p, tk, tv, grid, stream)
+                      : dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
+                                         : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
     if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
     if (wl.total) {

@@ -44,6 +44,7 @@ struct SplitParams {
   int chunk_fixed;               // > 0: rows per split chosen by the caller
   int chunk_min;                 // else: smallest rows per split the device may choose
   int max_splits;                // partial slots per query head (ceil(n_max / chunk))
+  float cta_speed;               // one CTA's streaming rate / its even share (split-length model)
   float scale_log2;              // scale * log2(e)
 };
 
@@ -201,6 +202,8 @@ __device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) {
   return __uint_as_float(x & 0xffff0000u);
 }
 
+__device__ __forceinline__ bool lane_is_zero(int tid) { return (tid & 31) == 0; }
+
 __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
   if (dev_error) atomicOr(dev_error, bit);
 }
@@ -211,12 +214,16 @@ __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
 struct KernelShape {
   int tile_rows;
   int heads_per_cta;
-  int box_cols;    // inner box width in elements
-  int swizzle128;  // 1: 128-byte swizzle, 0: none
+  int box_cols;     // inner box width in elements
+  int swizzle128;   // 1: 128-byte swizzle, 0: none
+  float cta_speed;  // how fast one CTA streams relative to an even share of HBM (measured)
 };
 
 KernelShape bf16_shape(int d, int group);
 KernelShape f32_shape(int d, int group);
+KernelShape tc5_shape(int group);
+cudaError_t launch_split_tc5(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             int grid, cudaStream_t stream);
 cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                               int d, int grid, cudaStream_t stream);
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -282,78 +289,74 @@ __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedu
   return it;
 }
 
-// Choose the split length when the caller left it to the library.  Candidates
-// are chunk_min * 2^k up to the first one covering the longest sequence.  For
-// each, the estimated time in "rows streamed by one CTA" is the larger of the
-// even share of all rows and the busiest CTA's rows (CTAs take items
-// round-robin; a CTA alone can stream ~1.6x its even share of HBM
-// bandwidth), plus one tile of epilogue per item and two tiles when partials
-// must be merged.  Warp 0 does the work (lane k scores candidate k, using
-// ceil(n / (a * 2^k)) = ceil(ceil(n / a) / 2^k)); all threads call this.
+// Choose the split length when the caller left it to the library.  Lanes
+// 0-15 of warp 0 score chunk_min * 2^k; lanes 16-31 score "balanced" lengths
+// that cut the longest sequence into R * grid / units pieces (R = 1..16), so
+// that the items fill whole rounds of the grid.  The estimated time in rows
+// streamed by one CTA is the larger of the even share of all rows and the
+// busiest CTA's rows divided by how fast one CTA can stream relative to its
+// even share (p.cta_speed: above 1 when a lone CTA can pull more than its
+// share of HBM bandwidth, below 1 when a CTA is compute-bound), plus one tile
+// of epilogue per item and two tiles when partials must be merged.  Ties go
+// to more, shorter items.  All threads call this.
 __device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* lens, int tile,
                                             int grid, int* red /* shared, >= 1 int */) {
   const int tid = threadIdx.x;
   if (tid < 32) {
-    const int lane = tid;
-    unsigned cnt[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) cnt[k] = 0;
+    const int k = tid;
     long long rows = 0;
     int nmax = 0;
-    for (int b = lane; b < p.B; b += 32) {
+    for (int b = 0; b < p.B; ++b) {
       const int n = len_of(lens[b]);
       rows += n;
       nmax = n > nmax ? n : nmax;
-      const unsigned u = n <= 0 ? 1u : unsigned((n + p.chunk_min - 1) / p.chunk_min);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const unsigned c = k < 31 ? (u + (1u << k) - 1u) >> k : 1u;
-        cnt[k] += c > 0u ? c : 1u;
-      }
-    }
-    // lane k ends up with the total for candidate k
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      unsigned v = cnt[k];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == k) cnt[0] = v;
-    }
-    const unsigned total_k = cnt[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      rows += __shfl_xor_sync(0xffffffffu, rows, o);
-      nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
     }
     const long long longest = nmax > 0 ? nmax : 1;
-    const int k = lane;
-    const long long c = (long long)p.chunk_min << k;
-    const long long cprev = k == 0 ? 0 : ((long long)p.chunk_min << (k - 1));
-    const bool candidate = k < 31 && cprev < longest;  // stop after the first covering one
+    const int per_seq = p.h_kv * p.head_chunks;
+    const long long units = (long long)p.B * per_seq;
+    long long c;
+    if (k < 16) {
+      c = (long long)p.chunk_min << k;
+    } else {
+      long long pieces = (long long)(k - 15) * grid / units;
+      if (pieces < 1) pieces = 1;
+      c = (longest + pieces - 1) / pieces;
+    }
+    c = (c + tile - 1) / tile * tile;
+    if (c < p.chunk_min) c = p.chunk_min;
+    if (c > (1LL << 30)) c = 1LL << 30;
+    // power-of-two candidates stop after the first one covering everything
+    const bool candidate = k >= 16 || k == 0 || ((long long)p.chunk_min << (k - 1)) < longest;
     float t = 3.0e38f;
     if (candidate) {
-      const int per_seq = p.h_kv * p.head_chunks;
-      const float items = float(total_k) * float(per_seq);
-      const float rounds = ceilf(items / float(grid));
+      long long items = 0;
+      const int ci = int(c);
+      for (int b = 0; b < p.B; ++b) {
+        const int n = len_of(lens[b]);
+        items += n <= 0 ? 1 : (n + ci - 1) / ci;
+      }
+      const float fitems = float(items) * float(per_seq);
+      const float rounds = ceilf(fitems / float(grid));
       const float share = float(rows) * float(per_seq) / float(grid);
       const float ceff = float(c < longest ? c : longest);
-      t = fmaxf(share, rounds * ceff * (1.f / 1.6f)) + rounds * float(tile);
+      t = fmaxf(share, rounds * ceff / p.cta_speed) + rounds * float(tile);
       if (c < longest) t += 2.f * float(tile);
     }
-    // argmin over lanes, ties (within 0.1%) to the smaller k (fewer items)
-    int best_k = k;
+    // argmin over lanes; within 0.1% prefer the shorter chunk (more items)
     float best_t = t;
+    long long best_c = c;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
-      const int ok = __shfl_xor_sync(0xffffffffu, best_k, o);
-      const bool take = ok < best_k ? ot <= best_t * 1.001f : ot * 1.001f < best_t;
+      const long long oc = __shfl_xor_sync(0xffffffffu, best_c, o);
+      const bool take = oc < best_c ? ot <= best_t * 1.001f
+                                    : (oc == best_c ? false : ot * 1.001f < best_t);
       if (take) {
         best_t = ot;
-        best_k = ok;
+        best_c = oc;
       }
     }
-    if (lane == 0) red[0] = int((long long)p.chunk_min << best_k);
+    if (k == 0) red[0] = int(best_c);
   }
   __syncthreads();
   const int chunk = red[0];
@@ -534,14 +537,14 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
       const int y0 = it.row_begin + t * TILE;
       const bool with_new = it.new_row >= y0 && it.new_row < y0 + TILE;
       uint32_t extra = 0;
-      if (t == 0) {
+      if (HEADS > 0 && t == 0) {
         const int h0 = it.hc * HEADS;
         const int nh = min(HEADS, p.group - h0);
         extra += uint32_t(nh) * ROW_BYTES;
       }
       if (with_new) extra += 2 * ROW_BYTES;
       mbar_arrive_expect_tx(bar, STAGE_BYTES + extra);
-      if (t == 0) {
+      if (HEADS > 0 && t == 0) {
         const int h0 = it.hc * HEADS;
         const int nh = min(HEADS, p.group - h0);
         const char* qsrc = static_cast<const char*>(p.q) +

@@ -362,23 +362,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 // Variant table and launcher.
 // ---------------------------------------------------------------------------
 using Bf16G8D128 = Bf16Cfg<128, 1, 1, 4, 2, 3>;
-using Bf16G16D128 = Bf16Cfg<128, 2, 1, 4, 1, 5>;
-using Bf16G32D128 = Bf16Cfg<128, 2, 2, 2, 2, 4>;
 using Bf16G8D64 = Bf16Cfg<64, 1, 1, 4, 2, 6>;
 using Bf16G16D64 = Bf16Cfg<64, 2, 1, 4, 1, 8>;
 using Bf16G32D64 = Bf16Cfg<64, 2, 2, 4, 1, 8>;
 
 template <class Cfg>
 static KernelShape shape_of() {
-  return KernelShape{Cfg::kTile, Cfg::kHeadsPerCta, 64, 1};
+  return KernelShape{Cfg::kTile, Cfg::kHeadsPerCta, 64, 1, 1.5f};
 }
 
 KernelShape bf16_shape(int d, int group) {
-  if (d == 128) {
-    if (group <= 8) return shape_of<Bf16G8D128>();
-    if (group <= 16) return shape_of<Bf16G16D128>();
-    return shape_of<Bf16G32D128>();
-  }
+  if (d == 128) return shape_of<Bf16G8D128>();  // larger groups use the tcgen05 kernel
   if (group <= 8) return shape_of<Bf16G8D64>();
   if (group <= 16) return shape_of<Bf16G16D64>();
   return shape_of<Bf16G32D64>();
@@ -401,11 +395,7 @@ static cudaError_t launch_cfg(const SplitParams& p, const CUtensorMap& tk, const
 
 cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                               int d, int grid, cudaStream_t stream) {
-  if (d == 128) {
-    if (p.group <= 8) return launch_cfg<Bf16G8D128>(p, tk, tv, grid, stream);
-    if (p.group <= 16) return launch_cfg<Bf16G16D128>(p, tk, tv, grid, stream);
-    return launch_cfg<Bf16G32D128>(p, tk, tv, grid, stream);
-  }
+  if (d == 128) return launch_cfg<Bf16G8D128>(p, tk, tv, grid, stream);
   if (p.group <= 8) return launch_cfg<Bf16G8D64>(p, tk, tv, grid, stream);
   if (p.group <= 16) return launch_cfg<Bf16G16D64>(p, tk, tv, grid, stream);
   return launch_cfg<Bf16G32D64>(p, tk, tv, grid, stream);

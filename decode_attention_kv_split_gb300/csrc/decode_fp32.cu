@@ -274,7 +274,7 @@ using F32G8 = F32Cfg<D, 8, 8, (D == 128 ? 32 : 64), 5>;
 
 template <class Cfg>
 static KernelShape f32_shape_of() {
-  return KernelShape{Cfg::kTile, Cfg::G, Cfg::D, 0};
+  return KernelShape{Cfg::kTile, Cfg::G, Cfg::D, 0, 1.5f};
 }
 
 template <int D>

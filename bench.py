@@ -54,7 +54,7 @@ def peaks():
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_kv_split_gb300", "csrc")
-    for fn in ("common.cuh", "decode_bf16.cu", "decode_fp32.cu"):   # the split kernels
+    for fn in ("common.cuh", "decode_bf16.cu", "decode_fp32.cu", "decode_tc5.cu"):  # split kernels
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]

@@ -91,7 +91,7 @@ DA_API int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v
 /*
  * Bytes of device workspace decode_attn_ex needs for this request: a 256-byte
  * header and the per-split partial outputs and log-sum-exps (float32) of at
- * most 1024 sequences (larger batches run as several launches that reuse
+ * most 512 sequences (larger batches run as several launches that reuse
  * it, one after the other on the stream).  0 when the request can only use
  * one split.  Returns 0 and sets *status (when non-NULL) to a
  * negative da_status if the arguments are invalid.
@@ -115,7 +115,7 @@ DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int
  *   dev_error    : nullable device int32; kernels OR DA_DEVERR_* bits into it
  *                  (it is never cleared by the library).
  *   stream       : CUDA stream for every launch.
- * Launches, per slice of at most 1024 sequences, one split kernel and, when
+ * Launches, per slice of at most 512 sequences, one split kernel and, when
  * more than one split may be used, one combine kernel (programmatic
  * dependent launch: it starts while the split kernel drains).
  */

@@ -118,8 +118,14 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.reader.join(timeout=2)
+        return self.summary(self.t0, self.t1)
+
+    def summary(self, t0, t1):
+        """Median SM clock and the throttle reasons seen between host times t0 and t1."""
+        if self.proc is None:
+            return None
         rows = []
-        for ts, line in self.lines:
+        for ts, line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue
@@ -129,7 +135,7 @@ class ClockSampler:
                 continue
         if not rows:
             return None
-        inwin = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e30)]
+        inwin = [r for r in rows if t0 is not None and t0 <= r[0] <= (t1 or 1e30)]
         use = inwin if inwin else rows
         sm = sorted(r[1] for r in use)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -257,57 +263,99 @@ def run_reference(args, w, world, rank):
 
 
 # --------------------------------------------------------------------------- our arm
+class Harness:
+    """Device-resident inputs of one workload and the step that the bench times."""
+
+    def __init__(self, w, rank: int, fused: bool, gpu_cache: bool = False):
+        from decode_attention_kv_split_gb300 import api
+
+        self.api = api
+        dev = torch.device("cuda", torch.cuda.current_device())
+        torch.manual_seed(rank)
+        n_max = w.n_max + CYCLE
+        wb = W.custom(name=w.name, B=w.B, h_q=w.h_q, h_kv=w.h_kv, d_k=w.d_k, d_v=w.d_v, n=w.n,
+                      n_max=n_max, dtype=w.dtype, kv_std=w.kv_std, ragged=w.ragged,
+                      num_splits=w.num_splits, description=w.description)
+        seed = 1000 * rank
+        lens0 = W.seq_lens(wb, seed)
+        es = 2 if w.dtype == torch.bfloat16 else 4
+        kv_touch = accounting.decode_bytes((lens0 + CYCLE).tolist(), w.h_q, w.h_kv, w.d_k, w.d_v,
+                                           es)
+        n_rot = max(1, math.ceil(4 * L2_BYTES / kv_touch))
+        cache_bytes = 2 * wb.B * wb.h_kv * n_max * wb.d_k * es
+        free = torch.cuda.mem_get_info(dev)[0]
+        n_rot = int(max(1, min(n_rot, 64, (0.6 * free) // cache_bytes)))
+
+        K0, V0 = W.cache(wb, seed, device=dev if gpu_cache else "cpu")
+        K0, V0 = K0.to(dev), V0.to(dev)
+        self.caches = [(K0, V0)] + [(K0.clone(), V0.clone()) for _ in range(n_rot - 1)]
+        del K0, V0
+        self.q = W.query(wb, seed).to(dev)
+        rows = [W.new_rows(wb, t, seed) for t in range(CYCLE)]
+        self.k_new = [k.to(dev) for k, _ in rows]
+        self.v_new = [v.to(dev) for _, v in rows]
+        self.pos_t = [(lens0 + t).to(torch.int32).to(dev) for t in range(CYCLE)]
+        self.lens_t = [(lens0 + t + 1).to(torch.int32).to(dev) for t in range(CYCLE)]
+        self.out = torch.empty((wb.B, wb.h_q, wb.d_v), dtype=torch.float32, device=dev)
+        self.splits = api.resolve_splits(wb.B, wb.h_q, wb.h_kv, wb.d_k, wb.d_v, n_max, wb.dtype,
+                                         w.num_splits)
+        ws_bytes = api.workspace_bytes(wb.B, wb.h_q, wb.h_kv, wb.d_k, wb.d_v, n_max, wb.dtype,
+                                       w.num_splits)
+        self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.w, self.wb, self.lens0, self.es = w, wb, lens0, es
+        self.n_rot, self.kv_touch, self.fused = n_rot, kv_touch, fused
+
+    def step(self, i, qq=None, kn=None, vn=None):
+        """One pass of the hot path: append row pos of every kv head, decode over pos+1."""
+        api, w = self.api, self.w
+        K, V = self.caches[i % self.n_rot]
+        c = i % CYCLE
+        qq = self.q if qq is None else qq
+        kn = self.k_new[c] if kn is None else kn
+        vn = self.v_new[c] if vn is None else vn
+        if self.fused:
+            api.decode_attn_append(qq, kn, vn, K, V, self.pos_t[c], out=self.out,
+                                   num_splits=w.num_splits, workspace=self.ws)
+        else:
+            api.kv_append(kn, vn, K, V, self.pos_t[c])
+            api.decode_attn(qq, K, V, self.lens_t[c], out=self.out, num_splits=w.num_splits,
+                            workspace=self.ws)
+
+    def step_bytes(self) -> int:
+        """Algorithmic HBM bytes of one step at the mean context of the 16-step cycle."""
+        w = self.w
+        mean_lens = [int(n) + (CYCLE + 1) / 2 for n in self.lens0.tolist()]
+        dec = accounting.decode_bytes(mean_lens, w.h_q, w.h_kv, w.d_k, w.d_v, self.es)
+        app = accounting.append_bytes(w.B, w.h_kv, w.d_k, w.d_v, self.es)
+        # the fused call reads the new row once (from k_new/v_new) and writes it once
+        return dec + app // 2 if self.fused else dec + app
+
+    def time_steps(self, K: int, world: int = 1) -> float:
+        """Device time in ms of K consecutive steps, from one CUDA event pair on the stream."""
+        ev_start = torch.cuda.Event(enable_timing=True)
+        ev_end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        # Keep the GPU busy (outside the timed region) while the host queues the
+        # first steps, so that host launch latency does not leak into the timing.
+        torch.cuda._sleep(int(5e7))
+        ev_start.record(self.stream)
+        for i in range(K):
+            self.step(i)
+        ev_end.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return ev_start.elapsed_time(ev_end)
+
+
 def run_ours(args, w, world, rank, local):
     from decode_attention_kv_split_gb300 import api
 
-    dev = torch.device("cuda", torch.cuda.current_device())
-    torch.manual_seed(rank)
-    n_max = w.n_max + CYCLE
-    wb = W.custom(name=w.name, B=w.B, h_q=w.h_q, h_kv=w.h_kv, d_k=w.d_k, d_v=w.d_v, n=w.n,
-                  n_max=n_max, dtype=w.dtype, kv_std=w.kv_std, ragged=w.ragged,
-                  num_splits=w.num_splits, description=w.description)
-    seed = 1000 * rank
-    lens0 = W.seq_lens(wb, seed)
-    es = 2 if w.dtype == torch.bfloat16 else 4
-    kv_touch = accounting.decode_bytes((lens0 + CYCLE).tolist(), w.h_q, w.h_kv, w.d_k, w.d_v, es)
-    n_rot = max(1, math.ceil(4 * L2_BYTES / kv_touch))
-    cache_bytes = 2 * wb.B * wb.h_kv * n_max * wb.d_k * es
-    free = torch.cuda.mem_get_info(dev)[0]
-    n_rot = int(max(1, min(n_rot, 64, (0.6 * free) // cache_bytes)))
-
-    K0, V0 = W.cache(wb, seed)
-    caches = []
-    for r in range(n_rot):
-        caches.append((K0.to(dev), V0.to(dev)))
-    del K0, V0
-    q = W.query(wb, seed).to(dev)
-    rows = [W.new_rows(wb, t, seed) for t in range(CYCLE)]
-    k_new = [k.to(dev) for k, _ in rows]
-    v_new = [v.to(dev) for _, v in rows]
-    pos_t = [(lens0 + t).to(torch.int32).to(dev) for t in range(CYCLE)]
-    lens_t = [(lens0 + t + 1).to(torch.int32).to(dev) for t in range(CYCLE)]
-    out = torch.empty((wb.B, wb.h_q, wb.d_v), dtype=torch.float32, device=dev)
-    splits = api.resolve_splits(wb.B, wb.h_q, wb.h_kv, wb.d_k, wb.d_v, n_max, wb.dtype, w.num_splits)
-    ws_bytes = api.workspace_bytes(wb.B, wb.h_q, wb.h_kv, wb.d_k, wb.d_v, n_max, wb.dtype, w.num_splits)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    fused = not args.separate_append
-
-    def step(i, qq=None, kn=None, vn=None):
-        """One pass of the hot path: append row pos of every kv head, decode over pos+1."""
-        K, V = caches[i % n_rot]
-        c = i % CYCLE
-        qq = q if qq is None else qq
-        kn = k_new[c] if kn is None else kn
-        vn = v_new[c] if vn is None else vn
-        if fused:
-            api.decode_attn_append(qq, kn, vn, K, V, pos_t[c], out=out, num_splits=w.num_splits,
-                                   workspace=ws)
-        else:
-            api.kv_append(kn, vn, K, V, pos_t[c])
-            api.decode_attn(qq, K, V, lens_t[c], out=out, num_splits=w.num_splits, workspace=ws)
-
+    h = Harness(w, rank, fused=not args.separate_append)
+    step, stream, fused, splits = h.step, h.stream, h.fused, h.splits
+    q, k_new, v_new, out = h.q, h.k_new, h.v_new, h.out
+    wb, n_rot, kv_touch = h.wb, h.n_rot, h.kv_touch
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -317,26 +365,14 @@ def run_ours(args, w, world, rank, local):
         sampler.start()
         time.sleep(0.3)
     K = args.steps
-    ev_start = torch.cuda.Event(enable_timing=True)
-    ev_end = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
     launches0 = api.launch_count()
     if sampler:
         sampler.mark(True)
-    # Keep the GPU busy (outside the timed region) while the host queues the
-    # first steps, so that host launch latency does not leak into the timing.
-    torch.cuda._sleep(int(5e7))
-    ev_start.record(stream)
-    for i in range(K):
-        step(i)
-    ev_end.record(stream)
-    torch.cuda.synchronize()
+    local_ms = h.time_steps(K, world)
     if sampler:
         sampler.mark(False)
-    barrier(world)
     launches = api.launch_count() - launches0
-    ms_per_step, tokens_per_s = replica_rate(ev_start.elapsed_time(ev_end), world, w.B, K)
+    ms_per_step, tokens_per_s = replica_rate(local_ms, world, w.B, K)
     clocks = sampler.stop() if sampler else None
 
     # ---- end to end: pinned host inputs in, result out, every step
@@ -373,17 +409,12 @@ def run_ours(args, w, world, rank, local):
     if rank != 0:
         return
     # ---- accounting
-    mean_lens = [int(n) + (CYCLE + 1) / 2 for n in lens0.tolist()]
-    dec_bytes = accounting.decode_bytes(mean_lens, w.h_q, w.h_kv, w.d_k, w.d_v, es)
-    app_bytes = accounting.append_bytes(w.B, w.h_kv, w.d_k, w.d_v, es)
-    # the fused call reads the new row once (from k_new/v_new) and writes it once
-    call_bytes = dec_bytes + app_bytes // 2 if fused else dec_bytes
+    step_bytes = h.step_bytes()
     peak, peak_kind = peaks()
-    step_bytes = call_bytes if fused else dec_bytes + app_bytes
     achieved = step_bytes / (ms_per_step / 1e3) / 1e9
     traffic = recorded_traffic(w.name)
     bytes_str = f"{step_bytes / 1e6:.1f} MB per step"
-    if w.B * w.h_kv * w.n * (w.d_k + w.d_v) * es < L2_BYTES:
+    if w.B * w.h_kv * w.n * (w.d_k + w.d_v) * h.es < L2_BYTES:
         bytes_str += " (L2-resident)"
 
     cpu_v, cpu_sample, cpu_cores = oracle_step_sample(wb, args.cpu_seconds, 1)
@@ -418,6 +449,48 @@ def run_ours(args, w, world, rank, local):
     print(json.dumps(line))
 
 
+SWEEP_CONTEXTS = (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
+SWEEP_SHAPES = ("gqa_llama3_8b", "mqa_g32", "long_llama2_70b", "mha_fp32")
+
+
+def run_sweep(args):
+    """Tokens/s and HBM GB/s against context length: every listed workload shape at
+    every context in ``--contexts``, all sequences at the same length, the fused step,
+    splits as ``--splits`` says (default: the library's choice).  One JSON line per
+    point; the K/V caches are drawn by a CUDA generator (timing only, no parity)."""
+    import dataclasses
+
+    peak, peak_kind = peaks()
+    contexts = [int(c) for c in args.contexts.split(",")]
+    shapes = args.sweep.split(",") if args.sweep != "all" else list(SWEEP_SHAPES)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    for name in shapes:
+        for n in contexts:
+            w = dataclasses.replace(W.WORKLOADS[name], n=n, n_max=n, ragged=None,
+                                    num_splits=args.splits or 0)
+            h = Harness(w, 0, fused=True, gpu_cache=True)
+            for i in range(args.warmup):
+                h.step(i)
+            probe_ms = h.time_steps(20) / 20
+            K = int(min(args.steps, max(50, 300.0 / probe_ms)))
+            t0 = time.time()
+            ms = h.time_steps(K) / K
+            clocks = sampler.summary(t0, time.time())
+            gbs = h.step_bytes() / (ms / 1e3) / 1e9
+            print(json.dumps({
+                "sweep": name, "context": f"{n + 1}..{n + CYCLE}", "n": n, "B": w.B,
+                "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d_k,
+                "kv_dtype": str(w.dtype).replace("torch.", ""), "steps": K,
+                "us_per_step": 1e3 * ms, "tokens_per_s": w.B / (ms / 1e3), "hbm_gbs": gbs,
+                "frac": gbs / peak, "peak": peak, "peak_kind": peak_kind,
+                "max_splits": h.splits, "n_rot": h.n_rot, "clocks": clocks}), flush=True)
+            del h
+            torch.cuda.empty_cache()
+    sampler.stop()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,6 +503,11 @@ def main():
                     help="run kv_append and decode_attn as two launches instead of the fused call")
     ap.add_argument("--splits", type=int, default=None,
                     help="override the workload's splits per sequence (0 = library's choice)")
+    ap.add_argument("--sweep", default=None,
+                    help="context sweep instead of the bench line: 'all' or a comma list of "
+                         "workload shapes")
+    ap.add_argument("--contexts", default=",".join(str(c) for c in SWEEP_CONTEXTS),
+                    help="contexts of the sweep (comma list)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -442,7 +520,11 @@ def main():
         run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")), rank)
         return
     world, rank, local = dist_setup()
-    run_ours(args, w, world, rank, local)
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+    else:
+        run_ours(args, w, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -18,20 +18,34 @@
 
 namespace da {
 
-// One CTA of 8 warps per (b, query head).  Warp w takes splits w, w+8, ...;
-// each lane holds D/32 consecutive columns.  The 8 partial sums meet in
-// shared memory.
+// One CTA of 16 warps per (b, query head).  Warp w merges splits w, w+16,
+// ... in one pass, four in flight, keeping a running maximum of the lse
+// values it has seen (the online form of the combine; every weight is taken
+// against the same maximum that scales the warp's sum).  Each lane holds D/32
+// consecutive columns.  The 16 warp results meet in shared memory and are
+// merged the same way.
+constexpr int kCombineWarps = 16;
+// Dynamic shared memory of one combine CTA.  Only the first
+// kCombineWarps * (D + 2) floats are used; the request is sized so that at
+// most two CTAs share an SM.  The grid may launch while the split kernel
+// drains, and without the cap its CTAs pile up on the first SMs to free up.
+constexpr int kCombineSmemBytes = 96 * 1024;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineWarps * 32)
     lse_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                        const int* __restrict__ chunk_in, const int32_t* __restrict__ seq_lens,
                        int append, float* __restrict__ out, int h_q, int max_splits, int n_max) {
   constexpr int EPL = D / 32;
-  constexpr int kWarps = 8;
-  __shared__ float red_m[kWarps];
-  __shared__ float red_w[kWarps];
-  __shared__ float red_acc[kWarps][D];
+  constexpr int kWarps = kCombineWarps;
+  extern __shared__ float csm[];
+  float* red_acc = csm;                 // [kWarps][D]
+  float* red_m = csm + kWarps * D;      // [kWarps]
+  float* red_w = red_m + kWarps;        // [kWarps]
 
+  // No early launch_dependents here: a next kernel whose CTAs sat resident
+  // beside these ones, waiting for this grid, slowed the merge.  It launches
+  // as these CTAs exit and waits for the grid to complete.
   wait_for_prerequisite_grid();
 
   const int bh = blockIdx.x;
@@ -46,80 +60,81 @@ __global__ void __launch_bounds__(256)
   const int nv = n <= 0 ? 1 : (n + chunk - 1) / chunk;
   if (nv <= 1 || chunk <= 0) return;  // written by the split kernel
   const float* lse = lse_part + size_t(bh) * max_splits;
-  const float* op = o_part + size_t(bh) * max_splits * D;
+  const float* op = o_part + size_t(bh) * max_splits * D + lane * EPL;
 
-  float mx = -INFINITY;
-  for (int s = threadIdx.x; s < nv; s += blockDim.x) mx = fmaxf(mx, __ldcg(lse + s));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red_m[warp] = mx;
-  __syncthreads();
-  float L = red_m[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) L = fmaxf(L, red_m[w]);
-
-  float acc[EPL];
+  float m = -INFINITY, wsum = 0.f, acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  int s = warp;
-  for (; s + 3 * kWarps < nv; s += 4 * kWarps) {  // four splits in flight per warp
-    float w[4], v[4][EPL];
+  for (int s = warp; s < nv; s += 4 * kWarps) {
+    float l[4], v[4][EPL];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      w[u] = __ldcg(lse + s + u * kWarps);
-      const float* row = op + size_t(s + u * kWarps) * D + lane * EPL;
+      const int su = s + u * kWarps;
+      const bool ok = su < nv;
+      l[u] = ok ? __ldcg(lse + su) : -INFINITY;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) v[u][e] = __ldcg(row + e);
+      for (int e = 0; e < EPL; ++e) v[u][e] = ok ? __ldcg(op + size_t(su) * D + e) : 0.f;
     }
+    const float mx = fmaxf(fmaxf(m, fmaxf(l[0], l[1])), fmaxf(l[2], l[3]));
+    const float m_use = mx == -INFINITY ? 0.f : mx;  // only empty splits so far
+    const float scale = ex2(m - m_use);              // 0 while m is -inf
+    wsum *= scale;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] *= scale;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float e2 = ex2(w[u] - L);
-      wsum += e2;
+      const float f = ex2(l[u] - m_use);
+      wsum += f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(e2, v[u][e], acc[e]);
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(f, v[u][e], acc[e]);
     }
+    m = mx;
   }
-  for (; s < nv; s += kWarps) {
-    const float e2 = ex2(__ldcg(lse + s) - L);
-    wsum += e2;
-    const float* row = op + size_t(s) * D + lane * EPL;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(e2, __ldcg(row + e), acc[e]);
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_w[warp] = wsum;
   }
-  if (lane == 0) red_w[warp] = wsum;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) red_acc[warp][lane * EPL + e] = acc[e];
+  for (int e = 0; e < EPL; ++e) red_acc[warp * D + lane * EPL + e] = acc[e];
   __syncthreads();
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w]);
+    const float M_use = M == -INFINITY ? 0.f : M;
     float W = 0.f, a = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      W += red_w[w];
-      a += red_acc[w][d];
+      const float f = ex2(red_m[w] - M_use);
+      W += f * red_w[w];
+      a += f * red_acc[w * D + d];
     }
     out[size_t(bh) * D + d] = W > 0.f ? a / W : 0.f;
   }
 }
 
+template <int D>
+static cudaError_t launch_combine_d(const float* o_part, const float* lse_part,
+                                    const int* chunk_in, const int32_t* seq_lens, int append,
+                                    float* out, int B, int h_q, int max_splits, int n_max,
+                                    cudaStream_t stream) {
+  static_assert(kCombineWarps * (D + 2) * 4 <= kCombineSmemBytes, "combine scratch");
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(lse_combine_kernel<D>, kCombineSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(lse_combine_kernel<D>, B * h_q, kCombineWarps * 32,
+                          size_t(kCombineSmemBytes), stream, o_part, lse_part, chunk_in, seq_lens,
+                          append, out, h_q, max_splits, n_max);
+}
+
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
                            const int32_t* seq_lens, int append, float* out, int B, int h_q, int d,
                            int max_splits, int n_max, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(B) * unsigned(h_q));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (d == 128)
-    return cudaLaunchKernelEx(&cfg, lse_combine_kernel<128>, o_part, lse_part, chunk_in, seq_lens,
-                              append, out, h_q, max_splits, n_max);
-  return cudaLaunchKernelEx(&cfg, lse_combine_kernel<64>, o_part, lse_part, chunk_in, seq_lens,
-                            append, out, h_q, max_splits, n_max);
+    return launch_combine_d<128>(o_part, lse_part, chunk_in, seq_lens, append, out, B, h_q,
+                                 max_splits, n_max, stream);
+  return launch_combine_d<64>(o_part, lse_part, chunk_in, seq_lens, append, out, B, h_q,
+                              max_splits, n_max, stream);
 }
 
 }  // namespace da

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/decode_attn.h"
 
 namespace da {
@@ -245,11 +247,28 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void
 // after another.  Persistent CTAs take items i = blockIdx.x + k * gridDim.x.
 // Every CTA builds the same list in shared memory from seq_lens.
 // ---------------------------------------------------------------------------
+// Shared-memory words of the work list: first[] and lens[] of up to
+// kMaxBatchPerLaunch sequences, reduction scratch for up to 16 warps, and the
+// decoded items 0 .. kItemCache-1 of the CTA (later items are decoded on the
+// fly).  Kernels reserve kSchedWords ints.
+constexpr int kItemCache = 64;
+constexpr int kItemWords = 8;
+constexpr int kSchedRedWords = 16 * 32 + 64;
+constexpr int kSchedLens = kMaxBatchPerLaunch + 1;          // offset of lens[]
+constexpr int kSchedRed = kSchedLens + kMaxBatchPerLaunch;  // offset of the scratch
+constexpr int kSchedItems = (kSchedRed + kSchedRedWords + 3) & ~3;
+constexpr int kSchedWords = kSchedItems + kItemCache * kItemWords;
+
 struct Schedule {
-  int* first;       // [B + 1] first item of sequence b (shared memory)
-  int* lens;        // [B] rows to decode; bit 31 set when row (len - 1) is appended now
+  int* w;           // kSchedWords ints of shared memory:
+                    //   [0, B]      first item of sequence b (first[B] = total)
+                    //   kSchedLens  rows to decode per sequence; bit 31 set when
+                    //               row (len - 1) is appended now
+                    //   kSchedItems this CTA's first items, decoded
   int chunk;
   int total;
+  __device__ __forceinline__ int first(int b) const { return w[b]; }
+  __device__ __forceinline__ int lens(int b) const { return w[kSchedLens + b]; }
 };
 
 constexpr int kAppendFlag = int(0x80000000u);
@@ -268,19 +287,20 @@ __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedu
   int lo = 0, hi = p.B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s.first[mid] <= i) lo = mid; else hi = mid - 1;
+    if (s.first(mid) <= i) lo = mid; else hi = mid - 1;
   }
   Item it;
   it.b = lo;
   const int per_seq = p.h_kv * p.head_chunks;
-  it.nv = (s.first[lo + 1] - s.first[lo]) / per_seq;
-  const int r = i - s.first[lo];
+  it.nv = (s.first(lo + 1) - s.first(lo)) / per_seq;
+  const int r = i - s.first(lo);
   const int unit = r / it.nv;
   it.split = r - unit * it.nv;
   it.kvh = unit / p.head_chunks;
   it.hc = unit - it.kvh * p.head_chunks;
-  const int n = len_of(s.lens[lo]);
-  it.new_row = (s.lens[lo] & kAppendFlag) ? n - 1 : -1;
+  const int lv = s.lens(lo);
+  const int n = len_of(lv);
+  it.new_row = (lv & kAppendFlag) ? n - 1 : -1;
   it.row_begin = it.split * s.chunk;
   const int end = it.row_begin + s.chunk;
   it.row_end = end < n ? end : n;
@@ -289,66 +309,90 @@ __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedu
   return it;
 }
 
-// Choose the split length when the caller left it to the library.  Lanes
-// 0-15 of warp 0 score chunk_min * 2^k; lanes 16-31 score "balanced" lengths
-// that cut the longest sequence into R * grid / units pieces (R = 1..16), so
-// that the items fill whole rounds of the grid.  The estimated time in rows
-// streamed by one CTA is the larger of the even share of all rows and the
-// busiest CTA's rows divided by how fast one CTA can stream relative to its
-// even share (p.cta_speed: above 1 when a lone CTA can pull more than its
-// share of HBM bandwidth, below 1 when a CTA is compute-bound), plus one tile
-// of epilogue per item and two tiles when partials must be merged.  Ties go
-// to more, shorter items.  All threads call this.
+// Item number i = blockIdx.x + k * gridDim.x of the work list: the k-th item
+// of this CTA, read back from shared memory when build_schedule decoded it.
+template <int TILE>
+__device__ __forceinline__ Item cta_item(const SplitParams& p, const Schedule& s, int i, int k) {
+  if (k >= kItemCache) return schedule_item<TILE>(p, s, i);
+  const int* w = s.w + kSchedItems + k * kItemWords;
+  Item it;
+  it.b = w[0];
+  it.kvh = w[1];
+  it.hc = w[2];
+  it.split = w[3];
+  it.nv = w[4];
+  it.row_begin = w[5];
+  it.row_end = w[6];
+  it.new_row = w[7];
+  it.tiles = (it.row_end - it.row_begin + TILE - 1) / TILE;
+  return it;
+}
+
+// Choose the split length when the caller left it to the library.  Lane k of
+// every warp stands for one candidate length: chunk_min * 2^k for k < 16, and
+// for k >= 16 the "balanced" length that cuts the longest sequence into
+// (k - 15) * grid / units pieces, so that the items fill whole rounds of the
+// grid.  The estimated time in rows streamed by one CTA is the larger of the
+// even share of all rows and the busiest CTA's rows divided by how fast one
+// CTA can stream relative to its even share (p.cta_speed: above 1 when a lone
+// CTA can pull more than its share of HBM bandwidth, below 1 when a CTA is
+// compute-bound), plus one tile of epilogue per item and two tiles when
+// partials must be merged.  Ties go to more, shorter items.  The item counts
+// are summed over the sequences by all warps of the CTA; every reduction runs
+// in a fixed order, so every CTA picks the same length.  All threads call this
+// with the CTA-wide row total and longest length.
 __device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* lens, int tile,
-                                            int grid, int* red /* shared, >= 1 int */) {
-  const int tid = threadIdx.x;
-  if (tid < 32) {
-    const int k = tid;
-    long long rows = 0;
-    int nmax = 0;
-    for (int b = 0; b < p.B; ++b) {
+                                            int grid, float rows, int nmax,
+                                            int* red /* shared, kSchedRedWords */) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int longest = nmax > 0 ? nmax : 1;
+  const int per_seq = p.h_kv * p.head_chunks;
+  const int units = p.B * per_seq;
+  const int k = lane;
+  long long c;
+  if (k < 16) {
+    c = (long long)p.chunk_min << k;
+  } else {
+    int pieces = (k - 15) * grid / units;
+    if (pieces < 1) pieces = 1;
+    c = longest / pieces + (longest % pieces != 0);
+  }
+  c = (c + tile - 1) / tile * tile;
+  if (c < p.chunk_min) c = p.chunk_min;
+  if (c > (1 << 30)) c = 1 << 30;
+  const int ci = int(c);
+  // power-of-two candidates stop after the first one covering everything
+  const bool candidate = k >= 16 || k == 0 || ((long long)p.chunk_min << (k - 1)) < longest;
+  int items = 0;
+  if (candidate) {
+    int b = warp;
+#pragma unroll 4
+    for (; b < p.B; b += nwarps) {
       const int n = len_of(lens[b]);
-      rows += n;
-      nmax = n > nmax ? n : nmax;
+      items += n <= 0 ? 1 : (n - 1) / ci + 1;
     }
-    const long long longest = nmax > 0 ? nmax : 1;
-    const int per_seq = p.h_kv * p.head_chunks;
-    const long long units = (long long)p.B * per_seq;
-    long long c;
-    if (k < 16) {
-      c = (long long)p.chunk_min << k;
-    } else {
-      long long pieces = (long long)(k - 15) * grid / units;
-      if (pieces < 1) pieces = 1;
-      c = (longest + pieces - 1) / pieces;
-    }
-    c = (c + tile - 1) / tile * tile;
-    if (c < p.chunk_min) c = p.chunk_min;
-    if (c > (1LL << 30)) c = 1LL << 30;
-    // power-of-two candidates stop after the first one covering everything
-    const bool candidate = k >= 16 || k == 0 || ((long long)p.chunk_min << (k - 1)) < longest;
+  }
+  red[warp * 32 + lane] = items;
+  __syncthreads();
+  if (warp == 0) {
+    long long all = 0;
+    for (int w = 0; w < nwarps; ++w) all += red[w * 32 + lane];
     float t = 3.0e38f;
     if (candidate) {
-      long long items = 0;
-      const int ci = int(c);
-      for (int b = 0; b < p.B; ++b) {
-        const int n = len_of(lens[b]);
-        items += n <= 0 ? 1 : (n + ci - 1) / ci;
-      }
-      const float fitems = float(items) * float(per_seq);
+      const float fitems = float(all) * float(per_seq);
       const float rounds = ceilf(fitems / float(grid));
-      const float share = float(rows) * float(per_seq) / float(grid);
-      const float ceff = float(c < longest ? c : longest);
+      const float share = rows * float(per_seq) / float(grid);
+      const float ceff = float(ci < longest ? ci : longest);
       t = fmaxf(share, rounds * ceff / p.cta_speed) + rounds * float(tile);
-      if (c < longest) t += 2.f * float(tile);
+      if (ci < longest) t += 2.f * float(tile);
     }
     // argmin over lanes; within 0.1% prefer the shorter chunk (more items)
     float best_t = t;
-    long long best_c = c;
+    int best_c = ci;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
-      const long long oc = __shfl_xor_sync(0xffffffffu, best_c, o);
+      const int oc = __shfl_xor_sync(0xffffffffu, best_c, o);
       const bool take = oc < best_c ? ot <= best_t * 1.001f
                                     : (oc == best_c ? false : ot * 1.001f < best_t);
       if (take) {
@@ -356,23 +400,28 @@ __device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* len
         best_c = oc;
       }
     }
-    if (k == 0) red[0] = int(best_c);
+    __syncwarp();
+    if (lane == 0) red[kSchedRedWords - 1] = best_c;
   }
   __syncthreads();
-  const int chunk = red[0];
-  __syncthreads();
-  return chunk;
+  return red[kSchedRedWords - 1];
 }
 
 // Builds the work list in shared memory; every thread of the CTA must call it.
-// `first` has room for kMaxBatchPerLaunch + 1 ints, `lens` for kMaxBatchPerLaunch,
-// `red` for 48 ints.
+// `sched` points at kSchedWords ints (16-byte aligned).  Reads seq_lens (and
+// writes seq_lens_out from CTA 0): call it after any wait for the grid that
+// produced them.
 template <int TILE>
-__device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* first, int* lens,
-                                                   int* red) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sched) {
+  int* first = sched;
+  int* lens = sched + kSchedLens;
+  int* red = sched + kSchedRed;
+  int* items = sched + kSchedItems;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   bool bad = false;
   bool bad_pos = false;
+  float rows = 0.f;  // only feeds the split-length model; summed in a fixed order
+  int nmax = 0;
   for (int b = tid; b < p.B; b += blockDim.x) {
     int n = __ldg(p.seq_lens + b);
     bool app = false;
@@ -386,15 +435,37 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* fi
     }
     if (app) ++n;
     lens[b] = app ? (n | kAppendFlag) : n;
+    rows += float(n);
+    nmax = n > nmax ? n : nmax;
     if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n;
   }
   if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
   if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
-  __syncthreads();
   Schedule s;
-  s.first = first;
-  s.lens = lens;
-  s.chunk = p.chunk_fixed > 0 ? p.chunk_fixed : choose_chunk(p, lens, TILE, gridDim.x, red);
+  s.w = sched;
+  if (p.chunk_fixed > 0) {
+    __syncthreads();
+    s.chunk = p.chunk_fixed;
+  } else {
+    // CTA-wide row total and longest length, summed in a fixed order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      rows += __shfl_xor_sync(0xffffffffu, rows, o);
+      nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
+    }
+    if (lane == 0) {
+      red[16 * 32 + warp] = __float_as_int(rows);
+      red[16 * 32 + 32 + warp] = nmax;
+    }
+    __syncthreads();
+    float all_rows = 0.f;
+    int all_max = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      all_rows += __int_as_float(red[16 * 32 + w]);
+      all_max = max(all_max, red[16 * 32 + 32 + w]);
+    }
+    s.chunk = choose_chunk(p, lens, TILE, gridDim.x, all_rows, all_max, red);
+  }
   // exclusive scan of items per sequence by warp 0
   const int per_seq = p.h_kv * p.head_chunks;
   if (tid < 32) {
@@ -404,7 +475,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* fi
       int c = 0;
       if (b < p.B) {
         const int n = len_of(lens[b]);
-        c = per_seq * (n <= 0 ? 1 : (n + s.chunk - 1) / s.chunk);
+        c = per_seq * (n <= 0 ? 1 : (n - 1) / s.chunk + 1);
       }
       int x = c;
 #pragma unroll
@@ -420,6 +491,21 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* fi
   __syncthreads();
   s.total = first[p.B];
   if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = s.chunk;
+  // decode this CTA's first items, one per thread
+  const int mine = s.total > int(blockIdx.x) ? (s.total - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+  if (tid < mine && tid < kItemCache) {
+    const Item it = schedule_item<TILE>(p, s, int(blockIdx.x) + tid * int(gridDim.x));
+    int* w = items + tid * kItemWords;
+    w[0] = it.b;
+    w[1] = it.kvh;
+    w[2] = it.hc;
+    w[3] = it.split;
+    w[4] = it.nv;
+    w[5] = it.row_begin;
+    w[6] = it.row_end;
+    w[7] = it.new_row;
+  }
+  __syncthreads();
   return s;
 }
 
@@ -441,32 +527,36 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
   constexpr int GC = HG * HPW;  // query heads of this item
   if (*abort_flag) return;
   const int head0 = it.hc * GC;  // group-local index of the item's first head
-  const size_t bh0 = (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group);
-  for (int idx = ctid; idx < GC * D; idx += nthreads) {
-    const int h = idx / D;  // head inside the item
-    const int d = idx - h * D;
-    if (head0 + h >= p.group) continue;
-    const int hg = h / HPW, hw = h - hg * HPW;
-    float M = -INFINITY;
+  const int nh = min(GC, p.group - head0);
+  const size_t bh0 = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + head0;
+  const bool single = it.nv == 1;
+  const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
+  float* dst0 = single ? p.out + bh0 * D : p.o_part + (bh0 * p.max_splits + it.split) * D;
+  for (int d = ctid; d < D; d += nthreads) {
+    // the heads are independent: unrolled, their loads and merges overlap
 #pragma unroll
-    for (int k = 0; k < KW; ++k) M = fmaxf(M, epi_m[(hg * KW + k) * HPW + hw]);
-    float L = 0.f, sum = 0.f;
-    if (M != -INFINITY) {
+    for (int h = 0; h < GC; ++h) {
+      const int hg = h / HPW, hw = h - hg * HPW;
+      float m[KW], M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KW; ++k) {
+        m[k] = epi_m[(hg * KW + k) * HPW + hw];
+        M = fmaxf(M, m[k]);
+      }
+      const float M_use = M == -INFINITY ? 0.f : M;  // an empty item: every l is 0
+      float L = 0.f, sum = 0.f;
 #pragma unroll
       for (int k = 0; k < KW; ++k) {
         const int sid = hg * KW + k;
-        const float f = ex2(epi_m[sid * HPW + hw] - M);
+        const float f = ex2(m[k] - M_use);
         L += f * epi_l[sid * HPW + hw];
         sum += f * epi_acc[(sid * HPW + hw) * SLOT_STRIDE + d];
       }
-    }
-    const float o = L > 0.f ? sum / L : 0.f;
-    const size_t bh = bh0 + head0 + h;
-    if (it.nv == 1) {
-      p.out[bh * D + d] = o;
-    } else {
-      p.o_part[(bh * p.max_splits + it.split) * D + d] = o;
-      if (d == 0) p.lse_part[bh * p.max_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
+      if (h < nh) {
+        dst0[h * stride + d] = L > 0.f ? __fdividef(sum, L) : 0.f;
+        if (!single && d == 0)
+          p.lse_part[(bh0 + h) * p.max_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
+      }
     }
   }
 }
@@ -501,6 +591,43 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Host: raise a kernel's dynamic shared-memory limit to `smem` on the current
+// device, once per device.  `done` holds one bit per device ordinal (< 64);
+// each kernel instantiation owns its own word.  Setting it twice is harmless.
+template <class... Params>
+cudaError_t set_smem_limit_once(void (*kernel)(Params...), size_t smem,
+                                std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
+}
+
+// Host: launch a kernel as a programmatic dependent of the work before it on
+// the stream.  It may start while that grid drains (once every CTA of it has
+// run griddepcontrol.launch_dependents, or exited) and must execute
+// griddepcontrol.wait before it reads anything that grid wrote or writes
+// anything it reads.
+template <class... Params, class... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(unsigned(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Producer: one thread streams every tile of the CTA's items into the ring.
 // NBOX boxes of BOX_COLS columns per tensor per stage, each BOX_BYTES long.
@@ -523,8 +650,8 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
   int stage = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool aborted = false;
-  for (int i = blockIdx.x; i < s.total && !aborted; i += gridDim.x) {
-    const Item it = schedule_item<TILE>(p, s, i);
+  for (int i = blockIdx.x, k = 0; i < s.total && !aborted; i += gridDim.x, ++k) {
+    const Item it = cta_item<TILE>(p, s, i, k);
     const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
     for (int t = 0; t < it.tiles; ++t) {
       if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {

@@ -34,7 +34,7 @@ struct F32Cfg {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kEpiAccFloats = W * G * D;
   static constexpr int kEpiMLFloats = 2 * W * G;
-  static constexpr int kSchedWords = (2 * kMaxBatchPerLaunch + 1 + 48 + 1) & ~1;
+  static constexpr int kSchedWords = da::kSchedWords;  // work list (common.cuh)
   static constexpr int kQBytes = G * D * 4;  // q rows of one item, per stage
   static constexpr int kNewBytes = 2 * D * 4;  // appended K and V rows, per stage
   static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes + kNewBytes) +
@@ -72,10 +72,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   float* epi_acc = reinterpret_cast<float*>(newslots + size_t(STAGES) * Cfg::kNewBytes);
   float* epi_m = epi_acc + Cfg::kEpiAccFloats;
   float* epi_l = epi_m + W * G;
-  int* sched_first = reinterpret_cast<int*>(epi_l + W * G);
-  int* sched_lens = sched_first + kMaxBatchPerLaunch + 1;
-  int* sched_red = sched_lens + kMaxBatchPerLaunch;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sched_first + Cfg::kSchedWords);
+  int* sched_words = reinterpret_cast<int*>(epi_l + W * G);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sched_words + Cfg::kSchedWords);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
   const uint32_t ring = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
@@ -92,7 +90,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  const Schedule sched = build_schedule<Cfg::kTile>(p, sched_first, sched_lens, sched_red);
+  if (threadIdx.x == 32) {  // the tensor maps do not depend on the preceding grid
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  // Launched as a programmatic dependent: the set-up above overlaps the tail
+  // of the previous grid on the stream, which may have produced seq_lens, q,
+  // the caches or the new rows.  Nothing before this line reads them.
+  wait_for_prerequisite_grid();
+  const Schedule sched = build_schedule<Cfg::kTile>(p, sched_words);
   allow_dependent_launch();
 
   // ------------------------------------------------------------------ producer
@@ -108,8 +114,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
 
-  for (int i = blockIdx.x; i < sched.total; i += gridDim.x) {
-    const Item it = schedule_item<Cfg::kTile>(p, sched, i);
+  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
+    const Item it = cta_item<Cfg::kTile>(p, sched, i, k);
 
     const int head_base = it.hc * G;  // group-local index of this item's first head
     // q (pre-multiplied by scale * log2(e) once loaded, so scores come out in
@@ -292,16 +298,11 @@ KernelShape f32_shape(int d, int group) {
 template <class Cfg>
 static cudaError_t launch_f32_cfg(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                   int grid, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(split_decode_f32_kernel<Cfg>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Cfg::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  split_decode_f32_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(split_decode_f32_kernel<Cfg>, Cfg::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(split_decode_f32_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, tk, tv,
+                          p);
 }
 
 template <int D>

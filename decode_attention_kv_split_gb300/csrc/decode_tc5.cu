@@ -164,7 +164,7 @@ struct Tc5Cfg {
   static constexpr int kRowBytes = D * 2;              // an appended row
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 3);  // + producer + 2 MMA issuers
-  static constexpr int kSchedWords = (2 * kMaxBatchPerLaunch + 1 + 48 + 1) & ~1;
+  static constexpr int kSchedWords = da::kSchedWords;  // work list (common.cuh)
   static constexpr int kRedGroup = 4 * (NH / 2) + 4;   // [4 quarters][NH/2] partials + 4 flags
   static constexpr int kRedFloats = 2 * 2 * kRedGroup; // two groups, double-buffered
   // kfull, kempty, vfull, vempty, s_full[2], p_full[2], pv_done[2], fin
@@ -191,8 +191,8 @@ __device__ __forceinline__ void produce_ring(const CUtensorMap* map, const void*
   int slot = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool aborted = false;
-  for (int i = blockIdx.x; i < s.total && !aborted; i += gridDim.x) {
-    const Item it = schedule_item<T>(p, s, i);
+  for (int i = blockIdx.x, k = 0; i < s.total && !aborted; i += gridDim.x, ++k) {
+    const Item it = cta_item<T>(p, s, i, k);
     const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
     for (int t = 0; t < it.tiles; ++t) {
       if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
@@ -246,10 +246,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   uint8_t* p_buf = qsw + Cfg::kQBytes;  // [2 buffers][kPBytes], 1024-aligned
   uint8_t* knew = p_buf + 2 * Cfg::kPBytes;                      // [KST] appended K rows
   uint8_t* vnew = knew + size_t(KST) * Cfg::kRowBytes;           // [VST] appended V rows
-  int* sched_first = reinterpret_cast<int*>(vnew + size_t(VST) * Cfg::kRowBytes);
-  int* sched_lens = sched_first + kMaxBatchPerLaunch + 1;
-  int* sched_red = sched_lens + kMaxBatchPerLaunch;
-  float* red = reinterpret_cast<float*>(sched_first + Cfg::kSchedWords);
+  int* sched_words = reinterpret_cast<int*>(vnew + size_t(VST) * Cfg::kRowBytes);
+  float* red = reinterpret_cast<float*>(sched_words + Cfg::kSchedWords);
   uint64_t* bars = reinterpret_cast<uint64_t*>(red + Cfg::kRedFloats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -288,8 +286,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tc5::alloc(smem_u32(tmem_slot), kTmemCols);
     tc5::relinquish();
   }
+  if (threadIdx.x == 32) {  // the tensor maps do not depend on the preceding grid
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  // Launched as a programmatic dependent: the set-up above overlaps the tail
+  // of the previous grid on the stream, which may have produced seq_lens, q,
+  // the caches or the new rows.  Nothing before this line reads them.
+  wait_for_prerequisite_grid();
   tc5::fence_before();
-  const Schedule sched = build_schedule<T>(p, sched_first, sched_lens, sched_red);
+  const Schedule sched = build_schedule<T>(p, sched_words);
   tc5::fence_after();
   allow_dependent_launch();
   const uint32_t tmem = *tmem_slot;
@@ -331,8 +337,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t idesc_s = tc5::idesc_bf16(128, NH, 0, 0);
       int kslot = 0;
       uint32_t kphase = 0;
-      for (int i = blockIdx.x; i < sched.total && !aborted; i += gridDim.x) {
-        const Item it = schedule_item<T>(p, sched, i);
+      for (int i = blockIdx.x, k = 0; i < sched.total && !aborted; i += gridDim.x, ++k) {
+        const Item it = cta_item<T>(p, sched, i, k);
         if (it.tiles == 0) continue;
         // Q of the item's NH heads, swizzled K-major (rows past the group are
         // zero).  The score MMAs of the previous stage are complete once the
@@ -408,8 +414,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t idesc_o = tc5::idesc_bf16(128, 2 * NH, 1, 0);
       int vslot = 0;
       uint32_t vphase = 0;
-      for (int i = blockIdx.x; i < sched.total && !aborted; i += gridDim.x) {
-        const Item it = schedule_item<T>(p, sched, i);
+      for (int i = blockIdx.x, k = 0; i < sched.total && !aborted; i += gridDim.x, ++k) {
+        const Item it = cta_item<T>(p, sched, i, k);
         for (int t = 0; t < it.tiles; ++t, ++j) {
           const uint32_t b = j & 1;
           if (!warp_wait(p_full0 + 8 * b, (j >> 1) & 1)) break;
@@ -505,8 +511,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
     tc5::fence_after();
   };
-  for (int i = blockIdx.x; i < sched.total; i += gridDim.x) {
-    const Item it = schedule_item<T>(p, sched, i);
+  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
+    const Item it = cta_item<T>(p, sched, i, k);
     const int head0 = it.hc * NH;
     const size_t bh0 = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + head0;
     const int nheads = min(NH, p.group - head0);
@@ -630,38 +636,51 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       if (lane == 0) gred[quarter * HT + h] = v;
     }
     named_bar_sync(bar_id, 128);
-    float L[HT];
+    float L[HT], inv_l[HT];
 #pragma unroll
-    for (int h = 0; h < HT; ++h) L[h] = gred[h] + gred[HT + h] + gred[2 * HT + h] + gred[3 * HT + h];
+    for (int h = 0; h < HT; ++h) {
+      L[h] = gred[h] + gred[HT + h] + gred[2 * HT + h] + gred[3 * HT + h];
+      inv_l[h] = L[h] > 0.f ? __fdividef(1.f, L[h]) : 0.f;
+    }
     float o[HT];
     if (it.tiles > 0 && !*abort_flag) {
-      float r1[HT], r2[HT], r3[HT];  // remainder part, the odd chain's two parts
+      // O^T = (even chain head + remainder) + (odd chain head + remainder)
+      float r1[HT];
       tc5::ld16x(o_col + hb + lane_base, o, HT);
       tc5::ld16x(o_col + NH + hb + lane_base, r1, HT);
-      tc5::ld16x(o_col + 2 * NH + hb + lane_base, r2, HT);
-      tc5::ld16x(o_col + 3 * NH + hb + lane_base, r3, HT);
       tc5::wait_ld();
 #pragma unroll
-      for (int h = 0; h < HT; ++h) o[h] = (o[h] + r1[h]) + (r2[h] + r3[h]);
+      for (int h = 0; h < HT; ++h) o[h] += r1[h];
+      float r2[HT];
+      tc5::ld16x(o_col + 2 * NH + hb + lane_base, r1, HT);
+      tc5::ld16x(o_col + 3 * NH + hb + lane_base, r2, HT);
+      tc5::wait_ld();
+#pragma unroll
+      for (int h = 0; h < HT; ++h) o[h] += r1[h] + r2[h];
     } else {
 #pragma unroll
       for (int h = 0; h < HT; ++h) o[h] = 0.f;
     }
     if (!*abort_flag) {
-      const int d = t_row;
+      // column d = t_row of every head of this thread's half: one 128-byte
+      // row segment per warp and head
+      const bool single = it.nv == 1;
+      const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
+      float* dst = single ? p.out + (bh0 + hb) * D + t_row
+                          : p.o_part + ((bh0 + hb) * p.max_splits + it.split) * D + t_row;
 #pragma unroll
-      for (int h = 0; h < HT; ++h) {
-        if (hb + h >= nheads) break;
-        const float val = L[h] > 0.f ? o[h] * (1.f / L[h]) : 0.f;
-        const size_t bh = bh0 + hb + h;
-        if (it.nv == 1) {
-          p.out[bh * D + d] = val;
-        } else {
-          p.o_part[(bh * p.max_splits + it.split) * D + d] = val;
-          if (d == 0)
-            p.lse_part[bh * p.max_splits + it.split] =
-                L[h] > 0.f ? m_run[h] + log2f(L[h]) : -INFINITY;
-        }
+      for (int h = 0; h < HT; ++h)
+        if (hb + h < nheads) dst[h * stride] = o[h] * inv_l[h];
+      if (!single && quarter == 0 && lane < HT && hb + lane < nheads) {
+        float m_h = m_run[0], l_h = L[0];
+#pragma unroll
+        for (int h = 1; h < HT; ++h)
+          if (lane == h) {
+            m_h = m_run[h];
+            l_h = L[h];
+          }
+        p.lse_part[(bh0 + hb + lane) * p.max_splits + it.split] =
+            l_h > 0.f ? m_h + log2f(l_h) : -INFINITY;
       }
     }
     // the next item's first P.V overwrites O: our TMEM reads are complete
@@ -685,16 +704,11 @@ KernelShape tc5_shape(int group) {
 template <class Cfg>
 static cudaError_t launch_tc5_cfg(const SplitParams& p, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(split_decode_tc5_kernel<Cfg>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Cfg::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  split_decode_tc5_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(split_decode_tc5_kernel<Cfg>, Cfg::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(split_decode_tc5_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, tk, tv,
+                          p);
 }
 
 cudaError_t launch_split_tc5(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

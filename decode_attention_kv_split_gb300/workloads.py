@@ -76,10 +76,10 @@ WORKLOADS: dict[str, Workload] = {
 }
 
 
-def _randn(shape, seed: int, std: float) -> torch.Tensor:
-    g = torch.Generator(device="cpu")
+def _randn(shape, seed: int, std: float, device="cpu") -> torch.Tensor:
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
-    t = torch.randn(*shape, generator=g, dtype=torch.float32)
+    t = torch.randn(*shape, generator=g, dtype=torch.float32, device=device)
     if std != 1.0:
         t.mul_(std)
     return t
@@ -95,15 +95,17 @@ def seq_lens(w: Workload, seed: int = 0) -> torch.Tensor:
     return torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
 
 
-def cache(w: Workload, seed: int = 0, poison: bool = False):
-    """K [B, h_kv, n_max, d_k] and V [B, h_kv, n_max, d_v] in ``w.dtype`` (CPU).
+def cache(w: Workload, seed: int = 0, poison: bool = False, device="cpu"):
+    """K [B, h_kv, n_max, d_k] and V [B, h_kv, n_max, d_v] in ``w.dtype``.
 
     Rows at or beyond each sequence's length are filled with NaN when
     ``poison`` is set (a cache's unused rows may hold anything), otherwise
-    they hold random values like the rest.
+    they hold random values like the rest.  ``device`` picks where the
+    generator runs: a CUDA generator draws other numbers than the CPU one
+    from the same seed, so parity inputs are always made on the CPU.
     """
-    K = _randn((w.B, w.h_kv, w.n_max, w.d_k), seed + 0, w.kv_std).to(w.dtype)
-    V = _randn((w.B, w.h_kv, w.n_max, w.d_v), seed + 1, w.kv_std).to(w.dtype)
+    K = _randn((w.B, w.h_kv, w.n_max, w.d_k), seed + 0, w.kv_std, device).to(w.dtype)
+    V = _randn((w.B, w.h_kv, w.n_max, w.d_v), seed + 1, w.kv_std, device).to(w.dtype)
     if poison:
         lens = seq_lens(w, seed)
         for b in range(w.B):

@@ -331,8 +331,21 @@ class Harness:
         # the fused call reads the new row once (from k_new/v_new) and writes it once
         return dec + app // 2 if self.fused else dec + app
 
-    def time_steps(self, K: int, world: int = 1) -> float:
-        """Device time in ms of K consecutive steps, from one CUDA event pair on the stream."""
+    def capture(self, K: int):
+        """Record K consecutive steps into one CUDA graph (the way a serving loop
+        removes the host launch cost).  Returns (graph, kernels per replay)."""
+        api = self.api
+        g = torch.cuda.CUDAGraph()
+        n0 = api.launch_count()
+        with torch.cuda.graph(g):
+            for i in range(K):
+                self.step(i)
+        torch.cuda.synchronize()
+        return g, api.launch_count() - n0
+
+    def time_steps(self, K: int, world: int = 1, graph=None) -> float:
+        """Device time in ms of K consecutive steps, from one CUDA event pair on the
+        stream: a replay of `graph` (K steps recorded by capture()), or K eager calls."""
         ev_start = torch.cuda.Event(enable_timing=True)
         ev_end = torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -341,8 +354,11 @@ class Harness:
         # first steps, so that host launch latency does not leak into the timing.
         torch.cuda._sleep(int(5e7))
         ev_start.record(self.stream)
-        for i in range(K):
-            self.step(i)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(K):
+                self.step(i)
         ev_end.record(self.stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -365,13 +381,19 @@ def run_ours(args, w, world, rank, local):
         sampler.start()
         time.sleep(0.3)
     K = args.steps
+    graph = None
+    if not args.eager:
+        graph, launches = h.capture(K)
+        h.time_steps(K, world, graph)  # first replay: uploads the graph
     launches0 = api.launch_count()
     if sampler:
         sampler.mark(True)
-    local_ms = h.time_steps(K, world)
+    local_ms = h.time_steps(K, world, graph)
     if sampler:
         sampler.mark(False)
-    launches = api.launch_count() - launches0
+    if args.eager:
+        launches = api.launch_count() - launches0
+    del graph
     ms_per_step, tokens_per_s = replica_rate(local_ms, world, w.B, K)
     clocks = sampler.stop() if sampler else None
 
@@ -444,6 +466,9 @@ def run_ours(args, w, world, rank, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "sync": "host waits for each step's result"},
         "gpu_launches": launches,
+        "launch": ("eager: one C-ABI call per step" if args.eager else
+                   "the K steps recorded once through the C-ABI into a CUDA graph, "
+                   "replayed once inside the timed region"),
         "clocks": clocks,
     }
     print(json.dumps(line))
@@ -475,8 +500,13 @@ def run_sweep(args):
                 h.step(i)
             probe_ms = h.time_steps(20) / 20
             K = int(min(args.steps, max(50, 300.0 / probe_ms)))
+            graph = None
+            if not args.eager:
+                graph, _ = h.capture(K)
+                h.time_steps(K, 1, graph)
             t0 = time.time()
-            ms = h.time_steps(K) / K
+            ms = h.time_steps(K, 1, graph) / K
+            del graph
             clocks = sampler.summary(t0, time.time())
             gbs = h.step_bytes() / (ms / 1e3) / 1e9
             print(json.dumps({
@@ -485,7 +515,8 @@ def run_sweep(args):
                 "kv_dtype": str(w.dtype).replace("torch.", ""), "steps": K,
                 "us_per_step": 1e3 * ms, "tokens_per_s": w.B / (ms / 1e3), "hbm_gbs": gbs,
                 "frac": gbs / peak, "peak": peak, "peak_kind": peak_kind,
-                "max_splits": h.splits, "n_rot": h.n_rot, "clocks": clocks}), flush=True)
+                "max_splits": h.splits, "n_rot": h.n_rot, "clocks": clocks,
+                "launch": "eager" if args.eager else "cuda graph"}), flush=True)
             del h
             torch.cuda.empty_cache()
     sampler.stop()
@@ -503,6 +534,8 @@ def main():
                     help="run kv_append and decode_attn as two launches instead of the fused call")
     ap.add_argument("--splits", type=int, default=None,
                     help="override the workload's splits per sequence (0 = library's choice)")
+    ap.add_argument("--eager", action="store_true",
+                    help="time K eager C-ABI calls instead of one CUDA-graph replay of them")
     ap.add_argument("--sweep", default=None,
                     help="context sweep instead of the bench line: 'all' or a comma list of "
                          "workload shapes")

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libdecode_attn.so")
 
 DA_FP32 = 0
 DA_BF16 = 1
+DA_OUT_BF16 = 0x100  # dtype flag: out is bfloat16
 DEVERR_SEQ_LEN = 1
 DEVERR_POS = 2
 DEVERR_TIMEOUT = 4
@@ -154,6 +155,19 @@ def workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_split
 _ws_cache: dict = {}
 
 
+def _out(out: torch.Tensor | None, out_dtype: torch.dtype | None, B: int, h_q: int, d_v: int,
+         device: torch.device) -> tuple[torch.Tensor, int]:
+    """The output tensor (allocated when None) and its dtype flag."""
+    if out is None:
+        out = torch.empty((B, h_q, d_v), dtype=out_dtype or torch.float32, device=device)
+    if (out.shape != (B, h_q, d_v) or out.dtype not in (torch.float32, torch.bfloat16)
+            or not out.is_contiguous() or out.device != device
+            or (out_dtype is not None and out.dtype != out_dtype)):
+        raise ValueError("out must be a contiguous float32 or bfloat16 tensor [B, h_q, d_v] "
+                         "on the query's device")
+    return out, (DA_OUT_BF16 if out.dtype == torch.bfloat16 else 0)
+
+
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
     if nbytes == 0:
         return None
@@ -168,8 +182,10 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
 def decode_attn(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, seq_lens: torch.Tensor,
                 out: torch.Tensor | None = None, scale: float | None = None, num_splits: int = 0,
                 workspace: torch.Tensor | None = None, dev_error: torch.Tensor | None = None,
-                stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Decode attention (calls ``decode_attn_ex``); returns ``out`` [B, h_q, d_v] float32.
+                stream: torch.cuda.Stream | None = None,
+                out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """Decode attention (calls ``decode_attn_ex``); returns ``out`` [B, h_q, d_v], float32
+    or bfloat16 (``out_dtype``, or the dtype of a given ``out``).
 
     ``scale`` defaults to 1/sqrt(d_k).  ``workspace`` (uint8 CUDA tensor) is
     allocated and cached per stream when not given.  ``dev_error`` is an
@@ -178,11 +194,8 @@ def decode_attn(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, seq_lens: tor
     B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
     if scale is None:
         scale = 1.0 / math.sqrt(d_k)
-    if out is None:
-        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
-    elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
-    dt = _DTYPES[q.dtype]
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, q.device)
+    dt = _DTYPES[q.dtype] | oflag
     lib = load()
     with _on_device(q):
         need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, q.dtype, num_splits)
@@ -201,7 +214,8 @@ def decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
                        seq_lens_out: torch.Tensor | None = None, scale: float | None = None,
                        num_splits: int = 0, workspace: torch.Tensor | None = None,
                        dev_error: torch.Tensor | None = None,
-                       stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+                       stream: torch.cuda.Stream | None = None,
+                       out_dtype: torch.dtype | None = None) -> torch.Tensor:
     """Append row seq_lens[b] of every kv head and decode over seq_lens[b] + 1 rows,
     in one launch (calls ``decode_attn_append``); returns ``out``."""
     B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
@@ -214,10 +228,7 @@ def decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
         raise ValueError("seq_lens_out must be an int32 tensor of shape [B]")
     if scale is None:
         scale = 1.0 / math.sqrt(d_k)
-    if out is None:
-        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
-    elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, q.device)
     lib = load()
     with _on_device(q):
         need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, q.dtype, num_splits)
@@ -226,29 +237,30 @@ def decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
         nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         st = lib.decode_attn_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V),
                                     _ptr(seq_lens), _ptr(seq_lens_out), _ptr(out), B, h_q, h_kv,
-                                    d_k, d_v, n_max, float(scale), _DTYPES[q.dtype],
+                                    d_k, d_v, n_max, float(scale), _DTYPES[q.dtype] | oflag,
                                     int(num_splits), _ptr(workspace), nbytes, _ptr(dev_error),
                                     _stream(q, stream))
     _check(st, "decode_attn_append")
     return out
 
 
-def decode_attn_owned(q, K, V, seq_lens, out=None, scale=None, stream=None) -> torch.Tensor:
+def decode_attn_owned(q, K, V, seq_lens, out=None, scale=None, stream=None,
+                      out_dtype=None) -> torch.Tensor:
     """Decode attention through ``decode_attn`` (library-owned workspace)."""
     B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
     if scale is None:
         scale = 1.0 / math.sqrt(d_k)
-    if out is None:
-        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, q.device)
     with _on_device(q):
         st = load().decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q, h_kv,
-                                d_k, d_v, n_max, float(scale), _DTYPES[q.dtype], _stream(q, stream))
+                                d_k, d_v, n_max, float(scale), _DTYPES[q.dtype] | oflag,
+                                _stream(q, stream))
     _check(st, "decode_attn")
     return out
 
 
 def decode_attn_noalloc(q, K, V, seq_lens, out=None, scale=None, num_splits: int = 0,
-                        dev_error=None, stream=None) -> torch.Tensor:
+                        dev_error=None, stream=None, out_dtype=None) -> torch.Tensor:
     """Decode attention through ``decode_attn_noalloc``: the split scratch is the
     library's own fixed device buffer, so nothing is allocated for it.  Calls
     whose kernels may overlap on the GPU share that buffer and must be
@@ -256,13 +268,11 @@ def decode_attn_noalloc(q, K, V, seq_lens, out=None, scale=None, num_splits: int
     B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
     if scale is None:
         scale = 1.0 / math.sqrt(d_k)
-    if out is None:
-        out = torch.empty((B, h_q, d_v), dtype=torch.float32, device=q.device)
-    elif out.shape != (B, h_q, d_v) or out.dtype != torch.float32 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous float32 tensor [B, h_q, d_v]")
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, q.device)
     with _on_device(q):
         st = load().decode_attn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(out), B, h_q,
-                                        h_kv, d_k, d_v, n_max, float(scale), _DTYPES[q.dtype],
+                                        h_kv, d_k, d_v, n_max, float(scale),
+                                        _DTYPES[q.dtype] | oflag,
                                         int(num_splits), _ptr(dev_error), _stream(q, stream))
     _check(st, "decode_attn_noalloc")
     return out

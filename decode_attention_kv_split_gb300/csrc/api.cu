@@ -145,8 +145,20 @@ int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int
 // ---------------------------------------------------------------------------
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The element type of q, K, V and whether `out` is bf16, from a dtype argument.
+struct DtypeArg {
+  int kv;        // DA_FP32 or DA_BF16
+  bool out_bf16;
+};
+bool parse_dtype(int dtype, DtypeArg* a) {
+  a->kv = dtype & 0xff;
+  a->out_bf16 = (dtype & DA_OUT_BF16) != 0;
+  return (dtype & ~(0xff | DA_OUT_BF16)) == 0 && (a->kv == DA_FP32 || a->kv == DA_BF16);
+}
+
 int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype) {
-  if (dtype != DA_FP32 && dtype != DA_BF16) return DA_ERR_DTYPE;
+  DtypeArg dt;
+  if (!parse_dtype(dtype, &dt)) return DA_ERR_DTYPE;
   if (B <= 0 || h_q <= 0 || h_kv <= 0 || n_max <= 0) return DA_ERR_SHAPE;
   if (h_q % h_kv != 0) return DA_ERR_SHAPE;
   if (n_max > (1 << 30)) return DA_ERR_SHAPE;
@@ -207,8 +219,9 @@ bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, 
 // the library chooses, the device picks the length from the actual sequence
 // lengths; the host only bounds it from below so that the partial outputs of
 // at most about 4 x SMs work items per launch need workspace.
-int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype, int requested, int sms,
+int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype_arg, int requested, int sms,
               Plan* pl) {
+  const int dtype = dtype_arg & 0xff;
   const int group = h_q / h_kv;
   pl->tc5 = dtype == DA_BF16 && d == 128 && group > 8;
   pl->ks = pl->tc5 ? da::tc5_shape(group)
@@ -269,13 +282,16 @@ OwnedWorkspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
 
 int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_lens,
-                      float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
-                      float scale, int dtype, int num_splits, void* workspace,
+                      void* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                      float scale, int dtype_arg, int num_splits, void* workspace,
                       size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream,
                       const void* k_new, const void* v_new, int32_t* seq_lens_out) {
   if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
-  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype);
+  int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype_arg);
   if (st != DA_OK) return st;
+  DtypeArg dta;
+  parse_dtype(dtype_arg, &dta);
+  const int dtype = dta.kv;
   if (!isfinite(scale)) return DA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
       (workspace && !aligned16(workspace)))
@@ -284,6 +300,7 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
   if ((st = current_device(&dev, &sms)) != DA_OK) return st;
   Plan pl;
   if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
+  const size_t out_es = dta.out_bf16 ? 2 : 4;
   const WorkspaceLayout wl = workspace_layout(pl, h_q, d_k);
   if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return DA_ERR_WORKSPACE;
 
@@ -298,7 +315,8 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     SplitParams p;
     p.q = static_cast<const char*>(q) + size_t(b0) * h_q * d_k * es;
     p.seq_lens = seq_lens + b0;
-    p.out = out + size_t(b0) * h_q * d_v;
+    p.out = static_cast<char*>(out) + size_t(b0) * h_q * d_v * out_es;
+    p.out_bf16 = dta.out_bf16 ? 1 : 0;
     p.o_part = wl.total ? reinterpret_cast<float*>(ws + wl.o_part) : nullptr;
     p.lse_part = wl.total ? reinterpret_cast<float*>(ws + wl.lse_part) : nullptr;
     p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
@@ -329,8 +347,8 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
     if (wl.total) {
-      err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.append, p.out, bn,
-                               h_q, d_v, pl.max_splits, n_max, stream);
+      err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.append, p.out,
+                               p.out_bf16, bn, h_q, d_v, pl.max_splits, n_max, stream);
       if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
       g_launches.fetch_add(1);
     }
@@ -384,7 +402,7 @@ size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, i
   return st == DA_OK ? workspace_layout(pl, h_q, d_k).total : 0;
 }
 
-int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens, float* out,
+int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens, void* out,
                    int B, int h_q, int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
                    int num_splits, void* workspace, size_t workspace_bytes, int32_t* dev_error,
                    cudaStream_t stream) {
@@ -394,7 +412,7 @@ int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* s
 }
 
 int decode_attn_append(const void* q, const void* k_new, const void* v_new, void* K, void* V,
-                       const int32_t* seq_lens, int32_t* seq_lens_out, float* out, int B, int h_q,
+                       const int32_t* seq_lens, int32_t* seq_lens_out, void* out, int B, int h_q,
                        int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
                        int num_splits, void* workspace, size_t workspace_bytes,
                        int32_t* dev_error, cudaStream_t stream) {
@@ -406,7 +424,7 @@ int decode_attn_append(const void* q, const void* k_new, const void* v_new, void
                     seq_lens_out);
 }
 
-int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens, float* out,
+int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens, void* out,
                 int B, int h_q, int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
                 cudaStream_t stream) {
   if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;

@@ -35,7 +35,8 @@ template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     lse_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                        const int* __restrict__ chunk_in, const int32_t* __restrict__ seq_lens,
-                       int append, float* __restrict__ out, int h_q, int max_splits, int n_max) {
+                       int append, void* __restrict__ out, int out_bf16, int h_q, int max_splits,
+                       int n_max) {
   constexpr int EPL = D / 32;
   constexpr int kWarps = kCombineWarps;
   extern __shared__ float csm[];
@@ -109,14 +110,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
       W += f * red_w[w];
       a += f * red_acc[w * D + d];
     }
-    out[size_t(bh) * D + d] = W > 0.f ? a / W : 0.f;
+    const float v = W > 0.f ? a / W : 0.f;
+    if (out_bf16) static_cast<__nv_bfloat16*>(out)[size_t(bh) * D + d] = __float2bfloat16_rn(v);
+    else static_cast<float*>(out)[size_t(bh) * D + d] = v;
   }
 }
 
 template <int D>
 static cudaError_t launch_combine_d(const float* o_part, const float* lse_part,
                                     const int* chunk_in, const int32_t* seq_lens, int append,
-                                    float* out, int B, int h_q, int max_splits, int n_max,
+                                    void* out, int out_bf16, int B, int h_q, int max_splits, int n_max,
                                     cudaStream_t stream) {
   static_assert(kCombineWarps * (D + 2) * 4 <= kCombineSmemBytes, "combine scratch");
   static std::atomic<unsigned long long> smem_set{0};
@@ -124,16 +127,17 @@ static cudaError_t launch_combine_d(const float* o_part, const float* lse_part,
   if (e != cudaSuccess) return e;
   return launch_dependent(lse_combine_kernel<D>, B * h_q, kCombineWarps * 32,
                           size_t(kCombineSmemBytes), stream, o_part, lse_part, chunk_in, seq_lens,
-                          append, out, h_q, max_splits, n_max);
+                          append, out, out_bf16, h_q, max_splits, n_max);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, int append, float* out, int B, int h_q, int d,
+                           const int32_t* seq_lens, int append, void* out, int out_bf16, int B,
+                           int h_q, int d,
                            int max_splits, int n_max, cudaStream_t stream) {
   if (d == 128)
-    return launch_combine_d<128>(o_part, lse_part, chunk_in, seq_lens, append, out, B, h_q,
-                                 max_splits, n_max, stream);
-  return launch_combine_d<64>(o_part, lse_part, chunk_in, seq_lens, append, out, B, h_q,
+    return launch_combine_d<128>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
+                                 h_q, max_splits, n_max, stream);
+  return launch_combine_d<64>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B, h_q,
                               max_splits, n_max, stream);
 }
 

@@ -26,7 +26,7 @@ constexpr int kMaxBatchPerLaunch = 512;
 struct SplitParams {
   const void* q;                 // [B, h_q, d]  (this launch's slice of the batch)
   const int32_t* seq_lens;       // [B]
-  float* out;                    // [B, h_q, d]
+  void* out;                     // [B, h_q, d] float32, or bf16 when out_bf16
   float* o_part;                 // [B, h_q, max_splits, d]  normalised partial outputs
   float* lse_part;               // [B, h_q, max_splits]     log2-domain log-sum-exp
   int* chunk_out;                // workspace word receiving the split length used (nullable)
@@ -39,6 +39,7 @@ struct SplitParams {
   void* v_cache;                 // V base
   int32_t* seq_lens_out;         // nullable: receives the lengths after the append
   int append;
+  int out_bf16;                  // out holds bf16 (rounded once from the fp32 result)
   int B, h_q, h_kv, group;       // group = h_q / h_kv
   int b_offset;                  // first sequence of this launch inside the tensor maps
   int n_max;
@@ -231,7 +232,7 @@ cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, int append, float* out, int B, int h_q, int d,
+                           const int32_t* seq_lens, int append, void* out, int out_bf16, int B, int h_q, int d,
                            int max_splits, int n_max, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void* V,
                              const int32_t* pos, int B, int h_kv, int row_bytes_k,
@@ -509,6 +510,12 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   return s;
 }
 
+// One element of the final output, rounded to bf16 when the caller asked for it.
+__device__ __forceinline__ void store_out(const SplitParams& p, size_t idx, float v) {
+  if (p.out_bf16) static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+  else static_cast<float*>(p.out)[idx] = v;
+}
+
 // ---------------------------------------------------------------------------
 // End of a work item, shared by every split kernel.
 //
@@ -531,7 +538,7 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
   const size_t bh0 = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + head0;
   const bool single = it.nv == 1;
   const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
-  float* dst0 = single ? p.out + bh0 * D : p.o_part + (bh0 * p.max_splits + it.split) * D;
+  const size_t base = single ? bh0 * D : (bh0 * p.max_splits + it.split) * D;
   for (int d = ctid; d < D; d += nthreads) {
     // the heads are independent: unrolled, their loads and merges overlap
 #pragma unroll
@@ -553,7 +560,9 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
         sum += f * epi_acc[(sid * HPW + hw) * SLOT_STRIDE + d];
       }
       if (h < nh) {
-        dst0[h * stride + d] = L > 0.f ? __fdividef(sum, L) : 0.f;
+        const float val = L > 0.f ? __fdividef(sum, L) : 0.f;
+        if (single) store_out(p, base + h * stride + d, val);
+        else p.o_part[base + h * stride + d] = val;
         if (!single && d == 0)
           p.lse_part[(bh0 + h) * p.max_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
       }

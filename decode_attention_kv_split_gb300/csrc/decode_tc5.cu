@@ -666,11 +666,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // row segment per warp and head
       const bool single = it.nv == 1;
       const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
-      float* dst = single ? p.out + (bh0 + hb) * D + t_row
-                          : p.o_part + ((bh0 + hb) * p.max_splits + it.split) * D + t_row;
+      const size_t base = single ? (bh0 + hb) * D + t_row
+                                 : ((bh0 + hb) * p.max_splits + it.split) * D + t_row;
 #pragma unroll
       for (int h = 0; h < HT; ++h)
-        if (hb + h < nheads) dst[h * stride] = o[h] * inv_l[h];
+        if (hb + h < nheads) {
+          if (single) store_out(p, base + h * stride, o[h] * inv_l[h]);
+          else p.o_part[base + h * stride] = o[h] * inv_l[h];
+        }
       if (!single && quarter == 0 && lane < HT && hb + lane < nheads) {
         float m_h = m_run[0], l_h = L[0];
 #pragma unroll

@@ -52,7 +52,7 @@ int scratch_address(void** addr) {
 }  // namespace
 
 extern "C" int decode_attn_noalloc(const void* q, const void* K, const void* V,
-                                   const int32_t* seq_lens, float* out, int B, int h_q, int h_kv,
+                                   const int32_t* seq_lens, void* out, int B, int h_q, int h_kv,
                                    int d_k, int d_v, int n_max, float scale, int dtype,
                                    int num_splits, int32_t* dev_error, cudaStream_t stream) {
   if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;

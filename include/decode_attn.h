@@ -18,7 +18,7 @@
  *     q   [B, h_q, d_k]            dtype
  *     K   [B, h_kv, n_max, d_k]    dtype   (row l of head (b, kv) at ((b*h_kv+kv)*n_max+l)*d_k)
  *     V   [B, h_kv, n_max, d_v]    dtype
- *     out [B, h_q, d_v]            float32
+ *     out [B, h_q, d_v]            float32, or bfloat16 when dtype carries DA_OUT_BF16
  *   Rows at or beyond seq_lens[b] are never used: they may hold anything,
  *   including NaN.  A sequence with seq_lens[b] == 0 yields out = 0.
  *
@@ -64,6 +64,13 @@ typedef enum {
   DA_ERR_DEVICE = -7,      /* the current device is not sm_103 (GB300) */
   DA_ERR_UNSUPPORTED = -8  /* valid request this build has no kernel for */
 } da_status;
+
+/*
+ * Flag OR-ed into the dtype argument of the decode entry points: `out` is
+ * bfloat16 (round to nearest even of the fp32 result) instead of float32.
+ * Split partials and the combine stay in float32; the result is rounded once.
+ */
+#define DA_OUT_BF16 0x100
 
 /* Bits the kernels OR into the optional device error word. */
 #define DA_DEVERR_SEQ_LEN 1 /* some seq_lens[b] outside [0, n_max]: clamped into range */
@@ -120,7 +127,7 @@ DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int
  * dependent launch: it starts while the split kernel drains).
  */
 DA_API int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens,
-                          float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                          void* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
                           float scale, int dtype, int num_splits, void* workspace,
                           size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream);
 
@@ -141,7 +148,7 @@ DA_API int decode_attn_ex(const void* q, const void* K, const void* V, const int
  *   size is decode_attn_workspace_bytes of the same request).
  */
 DA_API int decode_attn_append(const void* q, const void* k_new, const void* v_new, void* K, void* V,
-                              const int32_t* seq_lens, int32_t* seq_lens_out, float* out, int B,
+                              const int32_t* seq_lens, int32_t* seq_lens_out, void* out, int B,
                               int h_q, int h_kv, int d_k, int d_v, int n_max, float scale,
                               int dtype, int num_splits, void* workspace, size_t workspace_bytes,
                               int32_t* dev_error, cudaStream_t stream);
@@ -156,7 +163,7 @@ DA_API int decode_attn_append(const void* q, const void* k_new, const void* v_ne
  * and must be serialised by the caller; use decode_attn_ex otherwise.
  */
 DA_API int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens,
-                       float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                       void* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
                        float scale, int dtype, cudaStream_t stream);
 
 /*
@@ -185,7 +192,7 @@ DA_API int decode_attn(const void* q, const void* K, const void* V, const int32_
 #define DA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 DA_API int decode_attn_noalloc(const void* q, const void* K, const void* V, const int32_t* seq_lens,
-                               float* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                               void* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
                                float scale, int dtype, int num_splits, int32_t* dev_error,
                                cudaStream_t stream);
 

@@ -66,6 +66,8 @@ def test_argument_errors_return_before_touching_cuda(lib):
     assert _decode_ex(lib, n_max=0) == -2
     assert _decode_ex(lib, n_max=(1 << 30) + 1) == -2
     assert _decode_ex(lib, dtype=7) == -3                  # DA_ERR_DTYPE
+    assert _decode_ex(lib, dtype=0x200) == -3              # unknown flag bit
+    assert _decode_ex(lib, dtype=api.DA_OUT_BF16 | 7) == -3
     assert _decode_ex(lib, d_k=96, d_v=96) == -8           # DA_ERR_UNSUPPORTED
     assert _decode_ex(lib, d_k=64, d_v=128) == -8
     assert _decode_ex(lib, scale=float("nan")) == -2
@@ -78,9 +80,20 @@ def test_kv_append_argument_errors(lib):
     ok = P(16)
     assert lib.kv_append(None, ok, ok, ok, ok, 1, 1, 64, 64, 8, 0, None, None) == -1
     assert lib.kv_append(ok, ok, ok, ok, ok, 1, 1, 64, 64, 8, 5, None, None) == -3
+    # no output, so no output-type flag
+    assert lib.kv_append(ok, ok, ok, ok, ok, 1, 1, 64, 64, 8, api.DA_OUT_BF16, None, None) == -3
     assert lib.kv_append(ok, ok, ok, ok, ok, 0, 1, 64, 64, 8, 0, None, None) == -2
     assert lib.kv_append(ok, ok, ok, ok, ok, 1, 1, 6, 64, 8, 1, None, None) == -2   # 12-byte rows
     assert lib.kv_append(ok, P(20), ok, ok, ok, 1, 1, 64, 64, 8, 0, None, None) == -4
+
+
+def test_header_constants_match_binding():
+    text = open(os.path.join(HEADER_DIR, "decode_attn.h")).read()
+    defs = dict(re.findall(r"#define\s+(DA_\w+)\s+(0x[0-9a-fA-F]+|\d+)", text))
+    assert int(defs["DA_OUT_BF16"], 0) == api.DA_OUT_BF16
+    assert int(defs["DA_DEVERR_SEQ_LEN"], 0) == api.DEVERR_SEQ_LEN
+    assert int(defs["DA_DEVERR_POS"], 0) == api.DEVERR_POS
+    assert int(defs["DA_DEVERR_TIMEOUT"], 0) == api.DEVERR_TIMEOUT
 
 
 def test_no_fallback_when_library_missing(tmp_path, monkeypatch):

@@ -62,6 +62,12 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.oracle_kv_append.restype = I
     lib.oracle_causal_attention.argtypes = [P, P, P, I, I, I, I, D, P]
     lib.oracle_causal_attention.restype = I
+    lib.oracle_code_value.argtypes = [I, I]
+    lib.oracle_code_value.restype = D
+    lib.oracle_quantize_rows.argtypes = [P, I64, I, I, P, P]
+    lib.oracle_quantize_rows.restype = I
+    lib.oracle_dequant_rows.argtypes = [P, P, I64, I, I, P]
+    lib.oracle_dequant_rows.restype = I
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = I
     return lib
@@ -174,6 +180,35 @@ class Oracle:
         out = np.zeros((H, T, d_v), dtype=np.float64)
         _check(self.lib.oracle_causal_attention(_ptr(Q), _ptr(K), _ptr(V), H, T, d_k, d_v,
                                                 float(scale), _ptr(out)), "causal_attention")
+        return out
+
+    # ---- 8-bit caches (kind 1: int8, kind 2: fp8 e4m3; see decode_oracle.c)
+    def code_value(self, code: int, kind: int) -> float:
+        """The value one 8-bit code stands for."""
+        return float(self.lib.oracle_code_value(int(code), int(kind)))
+
+    def quantize(self, x, kind: int):
+        """Rows x [..., d] (float32) -> (codes uint8 [..., d], scales float32 [...])."""
+        x = _f32(x)
+        d = x.shape[-1]
+        rows = x.size // d
+        codes = np.zeros(x.shape, dtype=np.uint8)
+        scales = np.zeros(x.shape[:-1], dtype=np.float32)
+        _check(self.lib.oracle_quantize_rows(_ptr(x), rows, d, int(kind), _ptr(codes),
+                                             _ptr(scales)), "quantize_rows")
+        return codes, scales
+
+    def dequant(self, codes, scales, kind: int) -> np.ndarray:
+        """codes uint8 [..., d], scales float32 [...] -> values float64 [..., d]."""
+        codes = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+        scales = _f32(scales)
+        d = codes.shape[-1]
+        rows = codes.size // d
+        if scales.size != rows:
+            raise ValueError("one scale per row")
+        out = np.zeros(codes.shape, dtype=np.float64)
+        _check(self.lib.oracle_dequant_rows(_ptr(codes), _ptr(scales), rows, d, int(kind),
+                                            _ptr(out)), "dequant_rows")
         return out
 
     def max_threads(self) -> int:

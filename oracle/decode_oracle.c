@@ -278,6 +278,131 @@ int oracle_causal_attention(const float *Q, const float *K, const float *V,
     return ORACLE_OK;
 }
 
+/*
+ * 8-bit KV caches.  The page "Attention over the KV cache in the decode step"
+ * notes that an int8 or fp8 cache halves the bytes per cached row (and so
+ * doubles the arithmetic intensity); it gives no storage format.  The reading
+ * used here: every cached row of K (and of V) is d one-byte codes c[j] plus
+ * one float32 scale s, and represents the values s * value(c[j]).
+ *
+ *   kind 1, int8      value(c) = the two's-complement integer, -128 .. 127.
+ *   kind 2, fp8 e4m3  sign bit, 4 exponent bits E (bias 7), 3 mantissa bits M:
+ *                     E in 1..15:  (-1)^sign * 2^(E - 7) * (1 + M / 8)
+ *                     E = 0:       (-1)^sign * 2^-6 * (M / 8)   (subnormal)
+ *                     E = 15, M = 7 is NaN; there are no infinities, so the
+ *                     largest finite magnitude is 2^8 * 1.75 = 448.
+ *
+ * Quantizing a row x[0..d-1] of float32 values (absmax scaling):
+ *   a = max_j |x[j]|;  s = a / Q in float32 (Q = 127 for int8, 448 for e4m3),
+ *   and s = 0 when a = 0;
+ *   v[j] = x[j] / s in float32, clamped to [-Q, Q] (saturation);
+ *   c[j] = the code whose value is nearest v[j], ties to the even code
+ *          (int8: even integer; e4m3: even mantissa), keeping the sign of a
+ *          zero result; c[j] = 0 for every j when s = 0.
+ * x must be finite.
+ */
+
+/* The value a code stands for (kind 1: int8, kind 2: fp8 e4m3). */
+double oracle_code_value(int code, int kind)
+{
+    const unsigned c = (unsigned)code & 0xffu;
+    if (kind == 1)
+        return (double)(c >= 128 ? (int)c - 256 : (int)c);
+    const int sign = (c >> 7) & 1;
+    const int E = (c >> 3) & 15;
+    const int M = c & 7;
+    if (E == 15 && M == 7) return NAN;
+    double mag;
+    if (E == 0) mag = ldexp((double)M / 8.0, -6);
+    else mag = ldexp(1.0 + (double)M / 8.0, E - 7);
+    return sign ? -mag : mag;
+}
+
+/* Nearest e4m3 code to v (|v| <= 448), ties to the even mantissa; a zero keeps v's sign. */
+static unsigned e4m3_nearest(double v)
+{
+    const unsigned sign = (v < 0.0 || (v == 0.0 && signbit(v))) ? 0x80u : 0u;
+    const double a = fabs(v);  /* the caller has clamped |v| to 448 */
+    /* the binade of a: spacing 2^(e-3) for normal values, 2^-9 below 2^-6 */
+    int e = -6;
+    if (a >= ldexp(1.0, -6)) {
+        e = (int)floor(log2(a));
+        /* guard against log2 rounding at exact powers of two */
+        if (ldexp(1.0, e) > a) --e;
+        if (ldexp(1.0, e + 1) <= a) ++e;
+    }
+    const double step = ldexp(1.0, e - 3);
+    double q = a / step;              /* exact: a power-of-two division */
+    double r = floor(q);
+    const double frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    /* r counts steps of the binade: 8..16 for normal e, 0..8 for subnormal */
+    int E, M;
+    if (e == -6 && r < 8.0) {
+        E = 0;
+        M = (int)r;
+    } else {
+        if (r >= 16.0) {
+            r = 8.0;
+            ++e;
+        }
+        E = e + 7;
+        M = (int)r - 8;
+    }
+    return sign | ((unsigned)E << 3) | (unsigned)M;
+}
+
+/*
+ * Quantize rows x[rows][d] (float32) into codes[rows][d] and scales[rows]
+ * as described above.
+ */
+int oracle_quantize_rows(const float *x, int64_t rows, int d, int kind,
+                         uint8_t *codes, float *scales)
+{
+    if (!x || !codes || !scales || rows < 0 || d <= 0 || (kind != 1 && kind != 2))
+        return ORACLE_ERR_ARG;
+    const float Q = kind == 1 ? 127.0f : 448.0f;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * d;
+        uint8_t *cr = codes + r * d;
+        float a = 0.0f;
+        for (int j = 0; j < d; ++j) {
+            const float m = fabsf(xr[j]);
+            if (m > a) a = m;
+        }
+        const float s = a / Q;
+        scales[r] = s;
+        for (int j = 0; j < d; ++j) {
+            if (s == 0.0f) {
+                cr[j] = 0;
+                continue;
+            }
+            float v = xr[j] / s;
+            if (v > Q) v = Q;
+            if (v < -Q) v = -Q;
+            if (kind == 1) {
+                const double n = nearbyint((double)v);   /* ties to even */
+                cr[j] = (uint8_t)(int8_t)(int)n;
+            } else {
+                cr[j] = (uint8_t)e4m3_nearest((double)v);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Values of rows of codes: out[r][j] = scales[r] * value(codes[r][j]), in double. */
+int oracle_dequant_rows(const uint8_t *codes, const float *scales, int64_t rows, int d,
+                        int kind, double *out)
+{
+    if (!codes || !scales || !out || rows < 0 || d <= 0 || (kind != 1 && kind != 2))
+        return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int j = 0; j < d; ++j)
+            out[r * d + j] = (double)scales[r] * oracle_code_value(codes[r * d + j], kind);
+    return ORACLE_OK;
+}
+
 /* Number of OpenMP threads a parallel region may use (1 without OpenMP). */
 int oracle_max_threads(void)
 {

@@ -289,4 +289,109 @@ def pin_kv_append_rows(o):
         assert np.array_equal(V.view(np.uint8), V1.view(np.uint8))
 
 
+# ----------------------------------------------------------------- 8-bit caches
+# The fp8 e4m3 format is fixed by its definition (1 sign, 4 exponent bits with
+# bias 7, 3 mantissa bits, subnormals below 2^-6, S.1111.111 the only NaN, no
+# infinities); int8 by two's complement.  These pins use values that follow
+# from those definitions and PyTorch's own float8_e4m3fn implementation.
+
+def pin_e4m3_code_values(o):
+    """Values the e4m3 definition fixes, and all 256 codes against PyTorch's float8_e4m3fn."""
+    fixed = {0x00: 0.0, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0x08: 2.0 ** -6,
+             0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0xB8: -1.0, 0xFE: -448.0, 0x30: 0.5}
+    for c, v in fixed.items():
+        assert o.code_value(c, 2) == v, (hex(c), o.code_value(c, 2), v)
+    assert math.isnan(o.code_value(0x7F, 2)) and math.isnan(o.code_value(0xFF, 2))
+    assert math.copysign(1.0, o.code_value(0x80, 2)) == -1.0
+    try:
+        import torch
+    except ImportError:  # pragma: no cover - torch is part of the test image
+        return
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([o.code_value(c, 2) for c in range(256)])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), [hex(c) for c in np.nonzero(~same)[0]]
+
+
+def pin_int8_code_values(o):
+    """Two's complement: 0x7F = 127, 0x80 = -128, 0xFF = -1."""
+    for c in range(256):
+        want = c - 256 if c >= 128 else c
+        assert o.code_value(c, 1) == want, (c, o.code_value(c, 1))
+
+
+def pin_quantize_absmax_maps_to_limit(o):
+    """The largest |x| of a row becomes the code for +-Q, and its scale is absmax / Q."""
+    rng = _rng(40)
+    x = _normal(rng, 16, 64)
+    for kind, Q, top in ((1, 127, 0x7F), (2, 448, 0x7E)):
+        codes, scales = o.quantize(x, kind)
+        for r in range(x.shape[0]):
+            j = int(np.argmax(np.abs(x[r])))
+            assert scales[r] == np.float32(np.abs(x[r]).max()) / np.float32(Q)
+            want = top if x[r, j] > 0 else (0x81 if kind == 1 else 0xFE)
+            assert codes[r, j] == want, (kind, r, hex(codes[r, j]))
+
+
+def pin_quantize_round_trip_error(o):
+    """|s * value(c) - x| is at most half a code step times s (plus the division's rounding)."""
+    rng = _rng(41)
+    x = _normal(rng, 32, 128) * np.float32(3.0)
+    for kind in (1, 2):
+        codes, scales = o.quantize(x, kind)
+        back = o.dequant(codes, scales, kind)
+        for r in range(x.shape[0]):
+            s = float(scales[r])
+            v = np.abs(x[r].astype(np.float64)) / s
+            if kind == 1:
+                step = np.ones_like(v)
+            else:  # e4m3 spacing: 2^-9 below 2^-6, else 2^(floor(log2 v) - 3)
+                e = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+                step = 2.0 ** (e - 3)
+            bound = s * (0.5 * step + 1e-6 * v + 1e-12)
+            err = np.abs(back[r] - x[r].astype(np.float64))
+            assert np.all(err <= bound), (kind, r, float(np.max(err - bound)))
+
+
+def pin_quantize_ties_to_even(o):
+    """x / s exactly halfway between two codes goes to the even one."""
+    # int8: absmax 127 makes s = 1 exactly, so x / s = x
+    x = np.array([[127.0, 2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5] + [0.0] * 8], dtype=np.float32)
+    codes, scales = o.quantize(x, 1)
+    assert scales[0] == 1.0
+    assert list(codes[0, :8].view(np.int8)) == [127, 2, 4, -2, -4, 0, 0, 2]
+    # e4m3: absmax 448 makes s = 1.  In [8, 16) the step is 1: 8.5 lies halfway between
+    # 8 (M=0) and 9 (M=1) -> 8, 9.5 between 9 (M=1) and 10 (M=2) -> 10; in [16, 32) the
+    # step is 2: 17 -> 16; 2^-10 is half the first subnormal -> 0; 3 * 2^-10 lies between
+    # 2^-9 (M=1) and 2^-8 (M=2) -> 2^-8; 440 lies between 416 and 448, nearer 448.
+    x = np.array([[448.0, 8.5, 9.5, -8.5, 2.0 ** -10, 3 * 2.0 ** -10, 17.0, 440.0] + [0.0] * 8],
+                 dtype=np.float32)
+    codes, scales = o.quantize(x, 2)
+    assert scales[0] == 1.0
+    vals = [o.code_value(c, 2) for c in codes[0, :8]]
+    assert vals == [448.0, 8.0, 10.0, -8.0, 0.0, 2.0 ** -8, 16.0, 448.0], vals
+
+
+def pin_quantize_zero_row(o):
+    """An all-zero row has scale 0 and all-zero codes."""
+    x = np.zeros((2, 32), dtype=np.float32)
+    for kind in (1, 2):
+        codes, scales = o.quantize(x, kind)
+        assert np.all(codes == 0) and np.all(scales == 0)
+
+
+def pin_quantize_matches_torch_e4m3_cast(o):
+    """The e4m3 codes equal PyTorch's round-to-nearest-even cast of x / s (|x / s| <= 448)."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        return
+    rng = _rng(42)
+    x = _normal(rng, 64, 128)
+    codes, scales = o.quantize(x, 2)
+    v = np.clip(x / scales[:, None], -448.0, 448.0).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ref, codes), int((ref != codes).sum())
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

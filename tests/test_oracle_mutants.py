@@ -29,6 +29,19 @@ MUTANTS = [
     ("causal_mask_leaks_next", "S[i * T + j] = (j > i) ?", "S[i * T + j] = (j > i + 1) ?"),
     ("kv_row_stride_uses_dk_for_v", "V + row0 * d_v,", "V + row0 * d_k,"),
     ("q_offset_per_kv_head", "oracle_decode_head(q + u * d_k,", "oracle_decode_head(q + (u / group) * d_k,"),
+    ("e4m3_bias_8", "else mag = ldexp(1.0 + (double)M / 8.0, E - 7);",
+     "else mag = ldexp(1.0 + (double)M / 8.0, E - 8);"),
+    ("e4m3_subnormal_scale", "if (E == 0) mag = ldexp((double)M / 8.0, -6);",
+     "if (E == 0) mag = ldexp((double)M / 8.0, -7);"),
+    ("int8_unsigned", "return (double)(c >= 128 ? (int)c - 256 : (int)c);", "return (double)c;"),
+    ("e4m3_ties_up", "if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
+     "if (frac >= 0.5) r += 1.0;"),
+    ("int8_limit_128", "const float Q = kind == 1 ? 127.0f : 448.0f;",
+     "const float Q = kind == 1 ? 128.0f : 448.0f;"),
+    ("absmax_signed", "const float m = fabsf(xr[j]);", "const float m = xr[j];"),
+    ("int8_truncates", "const double n = nearbyint((double)v);", "const double n = trunc((double)v);"),
+    ("dequant_drops_scale", "out[r * d + j] = (double)scales[r] * oracle_code_value(",
+     "out[r * d + j] = oracle_code_value("),
 ]
 
 

@@ -20,12 +20,17 @@ LIB_PATH = os.path.join(_PKG, "libdecode_attn.so")
 
 DA_FP32 = 0
 DA_BF16 = 1
+DA_INT8 = 2          # 8-bit caches: one-byte codes + a float32 scale per cached row
+DA_FP8_E4M3 = 3
 DA_OUT_BF16 = 0x100  # dtype flag: out is bfloat16
 DEVERR_SEQ_LEN = 1
 DEVERR_POS = 2
 DEVERR_TIMEOUT = 4
 
 _DTYPES = {torch.float32: DA_FP32, torch.bfloat16: DA_BF16}
+# 8-bit caches are passed as torch.int8 / torch.float8_e4m3fn tensors of codes
+_Q8_DTYPES = {torch.int8: DA_INT8, torch.float8_e4m3fn: DA_FP8_E4M3}
+_ALL_DTYPES = {**_DTYPES, **_Q8_DTYPES}
 
 _lock = threading.Lock()
 _lib = None
@@ -47,6 +52,12 @@ SIGNATURES = {
     "decode_attn_status_string": (ctypes.c_char_p, [_I]),
     "decode_attn_last_cuda_error": (ctypes.c_char_p, []),
     "decode_attn_launch_count": (ctypes.c_uint64, []),
+    "decode_attn_q8_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
+                               _SZ, _P, _P]),
+    "decode_attn_q8_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                   _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
+    "kv_append_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "kv_quantize": (_I, [_P, _I, _P, _P, ctypes.c_longlong, _I, _I, _P]),
 }
 
 
@@ -129,8 +140,10 @@ def _cache_dims(q, K, V, seq_lens):
 
 
 def resolve_splits(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_splits: int = 0) -> int:
-    """Splits per (b, kv head) the library uses for this request (on the current device)."""
-    r = load().decode_attn_resolve_splits(B, h_q, h_kv, d_k, d_v, n_max, _DTYPES[dtype], num_splits)
+    """Splits per (b, kv head) the library uses for this request (on the current device).
+    ``dtype`` is the cache's element type (torch.int8 / torch.float8_e4m3fn: 8-bit caches)."""
+    r = load().decode_attn_resolve_splits(B, h_q, h_kv, d_k, d_v, n_max, _ALL_DTYPES[dtype],
+                                          num_splits)
     if r < 0:
         raise DecodeAttnError(r, "decode_attn_resolve_splits")
     return r
@@ -145,8 +158,8 @@ def workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype: torch.dtype, num_split
     if hit is not None:
         return hit
     st = ctypes.c_int(0)
-    n = load().decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, _DTYPES[dtype], num_splits,
-                                           ctypes.byref(st))
+    n = load().decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, _ALL_DTYPES[dtype],
+                                           num_splits, ctypes.byref(st))
     _check(st.value, "decode_attn_workspace_bytes")
     _ws_bytes_cache[key] = int(n)
     return int(n)
@@ -299,6 +312,127 @@ def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, K: torch.Tensor, V: torc
         st = load().kv_append(_ptr(k_new), _ptr(v_new), _ptr(K), _ptr(V), _ptr(pos), B, h_kv, d_k,
                               d_v, n_max, _DTYPES[K.dtype], _ptr(dev_error), _stream(K, stream))
     _check(st, "kv_append")
+
+
+# ----------------------------------------------------------------- 8-bit caches
+def _q8_dims(q, K, V, k_scale, v_scale, seq_lens):
+    if q.dim() != 3 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("expected q [B, h_q, d], K/V codes [B, h_kv, n_max, d]")
+    B, h_q, d_k = q.shape
+    Bk, h_kv, n_max, d_k2 = K.shape
+    if V.shape != K.shape or Bk != B or d_k2 != d_k:
+        raise ValueError("q, K and V shapes disagree")
+    if K.dtype not in _Q8_DTYPES or V.dtype != K.dtype:
+        raise ValueError("K and V must be torch.int8 or torch.float8_e4m3fn code tensors")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("q must be bfloat16 with an 8-bit cache")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.shape != (B, h_kv, n_max) or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be a float32 tensor [B, h_kv, n_max]")
+    if seq_lens.shape != (B,) or seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be an int32 tensor of shape [B]")
+    for name, t in (("q", q), ("K", K), ("V", V), ("k_scale", k_scale), ("v_scale", v_scale),
+                    ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return B, h_q, h_kv, d_k, d_k, n_max
+
+
+def kv_quantize(x: torch.Tensor, code_dtype: torch.dtype, stream=None):
+    """Rows x [..., d] (float32 or bfloat16, CUDA) -> (codes [..., d] of ``code_dtype``
+    (torch.int8 or torch.float8_e4m3fn), scales float32 [...]) by absmax scaling
+    (calls ``kv_quantize``)."""
+    if x.dtype not in _DTYPES or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 or bfloat16 CUDA tensor")
+    d = x.shape[-1]
+    codes = torch.empty(x.shape, dtype=code_dtype, device=x.device)
+    scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    with _on_device(x):
+        st = load().kv_quantize(_ptr(x), _DTYPES[x.dtype], _ptr(codes), _ptr(scales),
+                                x.numel() // d if d else 0, d, _Q8_DTYPES[code_dtype],
+                                _stream(x, stream))
+    _check(st, "kv_quantize")
+    return codes, scales
+
+
+def decode_attn_q8(q, K, V, k_scale, v_scale, seq_lens, out=None, scale=None, num_splits: int = 0,
+                   workspace=None, dev_error=None, stream=None, out_dtype=None) -> torch.Tensor:
+    """Decode over an 8-bit cache (calls ``decode_attn_q8_ex``): K, V codes
+    [B, h_kv, n_max, d] (torch.int8 or torch.float8_e4m3fn) with row scales
+    [B, h_kv, n_max]; q bf16 [B, h_q, d].  Returns ``out``."""
+    B, h_q, h_kv, d_k, d_v, n_max = _q8_dims(q, K, V, k_scale, v_scale, seq_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, q.device)
+    lib = load()
+    with _on_device(q):
+        need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, K.dtype, num_splits)
+        if workspace is None:
+            workspace = _workspace(q.device, need)
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.decode_attn_q8_ex(_ptr(q), _ptr(K), _ptr(V), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(seq_lens), _ptr(out), B, h_q, h_kv, d_k, d_v, n_max,
+                                   float(scale), _Q8_DTYPES[K.dtype] | oflag, int(num_splits),
+                                   _ptr(workspace), nbytes, _ptr(dev_error), _stream(q, stream))
+    _check(st, "decode_attn_q8_ex")
+    return out
+
+
+def decode_attn_q8_append(q, k_new, v_new, k_new_scale, v_new_scale, K, V, k_scale, v_scale,
+                          seq_lens, out=None, seq_lens_out=None, scale=None, num_splits: int = 0,
+                          workspace=None, dev_error=None, stream=None, out_dtype=None):
+    """Append the code rows k_new/v_new [B, h_kv, d] (scales [B, h_kv]) at row
+    seq_lens[b] of an 8-bit cache and decode over seq_lens[b] + 1 rows in one
+    launch (calls ``decode_attn_q8_append``).  Returns ``out``."""
+    B, h_q, h_kv, d_k, d_v, n_max = _q8_dims(q, K, V, k_scale, v_scale, seq_lens)
+    for name, t, shape, dt in (("k_new", k_new, (B, h_kv, d_k), K.dtype),
+                               ("v_new", v_new, (B, h_kv, d_v), K.dtype),
+                               ("k_new_scale", k_new_scale, (B, h_kv), torch.float32),
+                               ("v_new_scale", v_new_scale, (B, h_kv), torch.float32)):
+        if t.shape != shape or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor {list(shape)} of {dt}")
+    if seq_lens_out is not None and (seq_lens_out.shape != (B,) or seq_lens_out.dtype != torch.int32):
+        raise ValueError("seq_lens_out must be an int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, q.device)
+    lib = load()
+    with _on_device(q):
+        need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, K.dtype, num_splits)
+        if workspace is None:
+            workspace = _workspace(q.device, need)
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.decode_attn_q8_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_new_scale),
+                                       _ptr(v_new_scale), _ptr(K), _ptr(V), _ptr(k_scale),
+                                       _ptr(v_scale), _ptr(seq_lens), _ptr(seq_lens_out), _ptr(out),
+                                       B, h_q, h_kv, d_k, d_v, n_max, float(scale),
+                                       _Q8_DTYPES[K.dtype] | oflag, int(num_splits),
+                                       _ptr(workspace), nbytes, _ptr(dev_error), _stream(q, stream))
+    _check(st, "decode_attn_q8_append")
+    return out
+
+
+def kv_append_q8(k_new, v_new, k_new_scale, v_new_scale, K, V, k_scale, v_scale, pos,
+                 dev_error=None, stream=None) -> None:
+    """Write code row pos[b] and its scale into every (b, kv head) of an 8-bit cache."""
+    if K.dim() != 4 or V.shape != K.shape or K.dtype not in _Q8_DTYPES or V.dtype != K.dtype:
+        raise ValueError("K, V must be 8-bit code tensors [B, h_kv, n_max, d] of one dtype")
+    B, h_kv, n_max, d = K.shape
+    for name, t, shape, dt in (("k_new", k_new, (B, h_kv, d), K.dtype),
+                               ("v_new", v_new, (B, h_kv, d), K.dtype),
+                               ("k_new_scale", k_new_scale, (B, h_kv), torch.float32),
+                               ("v_new_scale", v_new_scale, (B, h_kv), torch.float32),
+                               ("k_scale", k_scale, (B, h_kv, n_max), torch.float32),
+                               ("v_scale", v_scale, (B, h_kv, n_max), torch.float32),
+                               ("pos", pos, (B,), torch.int32)):
+        if t.shape != shape or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor {list(shape)} of {dt}")
+    with _on_device(K):
+        st = load().kv_append_q8(_ptr(k_new), _ptr(v_new), _ptr(k_new_scale), _ptr(v_new_scale),
+                                 _ptr(K), _ptr(V), _ptr(k_scale), _ptr(v_scale), _ptr(pos), B, h_kv,
+                                 d, d, n_max, _Q8_DTYPES[K.dtype], _ptr(dev_error),
+                                 _stream(K, stream))
+    _check(st, "kv_append_q8")
 
 
 def launch_count() -> int:

@@ -96,6 +96,12 @@ std::mutex g_map_mu;
 int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int d, int n_max,
                               int heads, const KernelShape& ks);
 
+// Bytes per cached element of a cache type; kScaleMap marks the tensor map
+// of an 8-bit cache's row scales.
+constexpr int kScaleMap = 100;
+int elem_size(int dtype) { return dtype == DA_FP32 ? 4 : dtype == DA_BF16 ? 2 : 1; }
+bool is_q8(int dtype) { return dtype == DA_INT8 || dtype == DA_FP8_E4M3; }
+
 // A [rows_total = B*h_kv heads][n_max][d] cache viewed as a 3-D tensor
 // (innermost first): x = column, y = row inside a head, z = b*h_kv + head.
 int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int d, int n_max, int heads,
@@ -123,15 +129,29 @@ int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int
   EncodeTiledFn fn;
   int st = get_encoder(&fn);
   if (st != DA_OK) return st;
-  const int es = dtype == DA_BF16 ? 2 : 4;
-  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(n_max), cuuint64_t(heads)};
-  const cuuint64_t strides[2] = {cuuint64_t(d) * es, cuuint64_t(n_max) * d * es};
-  const cuuint32_t box[3] = {cuuint32_t(ks.box_cols), cuuint32_t(ks.tile_rows), 1};
+  CUresult r;
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, dtype == DA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                  3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  ks.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (dtype == kScaleMap) {
+    // row scales [heads][n_max] float32, one row of the tile per element
+    const cuuint64_t dims[2] = {cuuint64_t(n_max), cuuint64_t(heads)};
+    const cuuint64_t strides[1] = {cuuint64_t(n_max) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ks.tile_rows), 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const int es = elem_size(dtype);
+    const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(n_max), cuuint64_t(heads)};
+    const cuuint64_t strides[2] = {cuuint64_t(d) * es, cuuint64_t(n_max) * d * es};
+    const cuuint32_t box[3] = {cuuint32_t(ks.box_cols), cuuint32_t(ks.tile_rows), 1};
+    const CUtensorMapDataType ty = dtype == DA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dtype == DA_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    r = fn(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE,
+           ks.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) {
     snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
              int(r));
@@ -153,7 +173,8 @@ struct DtypeArg {
 bool parse_dtype(int dtype, DtypeArg* a) {
   a->kv = dtype & 0xff;
   a->out_bf16 = (dtype & DA_OUT_BF16) != 0;
-  return (dtype & ~(0xff | DA_OUT_BF16)) == 0 && (a->kv == DA_FP32 || a->kv == DA_BF16);
+  return (dtype & ~(0xff | DA_OUT_BF16)) == 0 &&
+         (a->kv == DA_FP32 || a->kv == DA_BF16 || a->kv == DA_INT8 || a->kv == DA_FP8_E4M3);
 }
 
 int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype) {
@@ -166,6 +187,7 @@ int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype
   if ((long long)B * h_q > 0x7fffffffLL) return DA_ERR_SHAPE;
   if (d_k != d_v) return DA_ERR_UNSUPPORTED;
   if (d_k != 64 && d_k != 128) return DA_ERR_UNSUPPORTED;
+  if (is_q8(dt.kv) && n_max % 4 != 0) return DA_ERR_SHAPE;  // row-scale tensor map stride
   return DA_OK;
 }
 
@@ -225,7 +247,8 @@ int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype_arg, int req
   const int group = h_q / h_kv;
   pl->tc5 = dtype == DA_BF16 && d == 128 && group > 8;
   pl->ks = pl->tc5 ? da::tc5_shape(group)
-                   : (dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group));
+           : is_q8(dtype) ? da::q8_shape(d)
+                          : (dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group));
   pl->head_chunks = (group + pl->ks.heads_per_cta - 1) / pl->ks.heads_per_cta;
   pl->batch_per_launch = B < da::kMaxBatchPerLaunch ? B : da::kMaxBatchPerLaunch;
   const long long tile = pl->ks.tile_rows;
@@ -281,17 +304,31 @@ struct OwnedWorkspace {
 OwnedWorkspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
 
+// Row scales of an 8-bit cache (and of the appended rows, for a fused append).
+struct QuantArgs {
+  float* k_scale;
+  float* v_scale;
+  const float* k_new_scale;
+  const float* v_new_scale;
+};
+
 int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_lens,
                       void* out, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
                       float scale, int dtype_arg, int num_splits, void* workspace,
                       size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream,
-                      const void* k_new, const void* v_new, int32_t* seq_lens_out) {
+                      const void* k_new, const void* v_new, int32_t* seq_lens_out,
+                      const QuantArgs* qa) {
   if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
   int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype_arg);
   if (st != DA_OK) return st;
   DtypeArg dta;
   parse_dtype(dtype_arg, &dta);
   const int dtype = dta.kv;
+  // 8-bit caches go through the entry points that carry their row scales
+  if (is_q8(dtype) != (qa != nullptr)) return DA_ERR_DTYPE;
+  if (qa && (!qa->k_scale || !qa->v_scale || (k_new && (!qa->k_new_scale || !qa->v_new_scale))))
+    return DA_ERR_NULL;
+  if (qa && (!aligned16(qa->k_scale) || !aligned16(qa->v_scale))) return DA_ERR_ALIGN;
   if (!isfinite(scale)) return DA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
       (workspace && !aligned16(workspace)))
@@ -304,16 +341,23 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
   const WorkspaceLayout wl = workspace_layout(pl, h_q, d_k);
   if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return DA_ERR_WORKSPACE;
 
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tks, tvs;
   if ((st = encode_cache_map(&tk, K, dtype, d_k, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
   if ((st = encode_cache_map(&tv, V, dtype, d_v, n_max, B * h_kv, pl.ks)) != DA_OK) return st;
+  if (qa) {
+    if ((st = encode_cache_map(&tks, qa->k_scale, kScaleMap, 1, n_max, B * h_kv, pl.ks)) != DA_OK)
+      return st;
+    if ((st = encode_cache_map(&tvs, qa->v_scale, kScaleMap, 1, n_max, B * h_kv, pl.ks)) != DA_OK)
+      return st;
+  }
 
-  const int es = dtype == DA_BF16 ? 2 : 4;
+  const int es = elem_size(dtype);          // cached (and appended) elements
+  const int q_es = qa ? 2 : es;             // q is bf16 with an 8-bit cache
   char* ws = static_cast<char*>(workspace);
   for (int b0 = 0; b0 < B; b0 += pl.batch_per_launch) {
     const int bn = (B - b0) < pl.batch_per_launch ? (B - b0) : pl.batch_per_launch;
     SplitParams p;
-    p.q = static_cast<const char*>(q) + size_t(b0) * h_q * d_k * es;
+    p.q = static_cast<const char*>(q) + size_t(b0) * h_q * d_k * q_es;
     p.seq_lens = seq_lens + b0;
     p.out = static_cast<char*>(out) + size_t(b0) * h_q * d_v * out_es;
     p.out_bf16 = dta.out_bf16 ? 1 : 0;
@@ -327,6 +371,10 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.k_cache = const_cast<void*>(K);
     p.v_cache = const_cast<void*>(V);
     p.seq_lens_out = seq_lens_out ? seq_lens_out + b0 : nullptr;
+    p.k_scale = qa ? qa->k_scale : nullptr;
+    p.v_scale = qa ? qa->v_scale : nullptr;
+    p.k_new_scale = qa && qa->k_new_scale ? qa->k_new_scale + size_t(b0) * h_kv : nullptr;
+    p.v_new_scale = qa && qa->v_new_scale ? qa->v_new_scale + size_t(b0) * h_kv : nullptr;
     p.B = bn;
     p.h_q = h_q;
     p.h_kv = h_kv;
@@ -341,9 +389,11 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
     const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
     const int grid = int(items < sms ? items : sms);
-    cudaError_t err = pl.tc5 ? da::launch_split_tc5(p, tk, tv, grid, stream)
-                      : dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
-                                         : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
+    cudaError_t err =
+        pl.tc5 ? da::launch_split_tc5(p, tk, tv, grid, stream)
+        : qa   ? da::launch_split_q8(p, tk, tv, tks, tvs, d_k, dtype == DA_INT8 ? 1 : 2, grid, stream)
+        : dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
+                           : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
     if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
     if (wl.total) {
@@ -408,7 +458,7 @@ int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* s
                    cudaStream_t stream) {
   return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
                     num_splits, workspace, workspace_bytes, dev_error, stream, nullptr, nullptr,
-                    nullptr);
+                    nullptr, nullptr);
 }
 
 int decode_attn_append(const void* q, const void* k_new, const void* v_new, void* K, void* V,
@@ -421,7 +471,7 @@ int decode_attn_append(const void* q, const void* k_new, const void* v_new, void
   if (seq_lens_out && seq_lens_out == seq_lens) return DA_ERR_SHAPE;
   return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
                     num_splits, workspace, workspace_bytes, dev_error, stream, k_new, v_new,
-                    seq_lens_out);
+                    seq_lens_out, nullptr);
 }
 
 int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens, void* out,
@@ -462,13 +512,14 @@ int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_
                         need, nullptr, stream);
 }
 
-int kv_append(const void* k_new, const void* v_new, void* K, void* V, const int32_t* pos, int B,
-              int h_kv, int d_k, int d_v, int n_max, int dtype, int32_t* dev_error,
-              cudaStream_t stream) {
+namespace {
+int append_rows(const void* k_new, const void* v_new, void* K, void* V, const int32_t* pos, int B,
+                int h_kv, int d_k, int d_v, int n_max, int dtype, const float* ks_new,
+                const float* vs_new, float* ks, float* vs, int32_t* dev_error,
+                cudaStream_t stream) {
   if (!k_new || !v_new || !K || !V || !pos) return DA_ERR_NULL;
-  if (dtype != DA_FP32 && dtype != DA_BF16) return DA_ERR_DTYPE;
   if (B <= 0 || h_kv <= 0 || d_k <= 0 || d_v <= 0 || n_max <= 0) return DA_ERR_SHAPE;
-  const int es = dtype == DA_BF16 ? 2 : 4;
+  const int es = elem_size(dtype);
   if ((d_k * es) % 16 != 0 || (d_v * es) % 16 != 0) return DA_ERR_SHAPE;
   if ((long long)B * h_kv * (long long)n_max > 0x7fffffffLL) return DA_ERR_SHAPE;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(K) || !aligned16(V)) return DA_ERR_ALIGN;
@@ -476,8 +527,72 @@ int kv_append(const void* k_new, const void* v_new, void* K, void* V, const int3
   int st = current_device(&dev, &sms);
   if (st != DA_OK) return st;
   cudaError_t e = da::launch_kv_append(k_new, v_new, K, V, pos, B, h_kv, d_k * es, d_v * es, n_max,
-                                       dev_error, stream);
+                                       ks_new, vs_new, ks, vs, dev_error, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kv_append launch");
+  g_launches.fetch_add(1);
+  return DA_OK;
+}
+}  // namespace
+
+int kv_append(const void* k_new, const void* v_new, void* K, void* V, const int32_t* pos, int B,
+              int h_kv, int d_k, int d_v, int n_max, int dtype, int32_t* dev_error,
+              cudaStream_t stream) {
+  if (dtype != DA_FP32 && dtype != DA_BF16) return DA_ERR_DTYPE;
+  return append_rows(k_new, v_new, K, V, pos, B, h_kv, d_k, d_v, n_max, dtype, nullptr, nullptr,
+                     nullptr, nullptr, dev_error, stream);
+}
+
+int kv_append_q8(const void* k_new, const void* v_new, const float* k_new_scale,
+                 const float* v_new_scale, void* K, void* V, float* k_scale, float* v_scale,
+                 const int32_t* pos, int B, int h_kv, int d_k, int d_v, int n_max, int dtype,
+                 int32_t* dev_error, cudaStream_t stream) {
+  if (!is_q8(dtype)) return DA_ERR_DTYPE;
+  if (!k_new_scale || !v_new_scale || !k_scale || !v_scale) return DA_ERR_NULL;
+  return append_rows(k_new, v_new, K, V, pos, B, h_kv, d_k, d_v, n_max, dtype, k_new_scale,
+                     v_new_scale, k_scale, v_scale, dev_error, stream);
+}
+
+int decode_attn_q8_ex(const void* q, const void* K, const void* V, const float* k_scale,
+                      const float* v_scale, const int32_t* seq_lens, void* out, int B, int h_q,
+                      int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
+                      int num_splits, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_error, cudaStream_t stream) {
+  if (!is_q8(dtype & 0xff)) return DA_ERR_DTYPE;
+  const QuantArgs qa{const_cast<float*>(k_scale), const_cast<float*>(v_scale), nullptr, nullptr};
+  return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
+                    num_splits, workspace, workspace_bytes, dev_error, stream, nullptr, nullptr,
+                    nullptr, &qa);
+}
+
+int decode_attn_q8_append(const void* q, const void* k_new, const void* v_new,
+                          const float* k_new_scale, const float* v_new_scale, void* K, void* V,
+                          float* k_scale, float* v_scale, const int32_t* seq_lens,
+                          int32_t* seq_lens_out, void* out, int B, int h_q, int h_kv, int d_k,
+                          int d_v, int n_max, float scale, int dtype, int num_splits,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_error,
+                          cudaStream_t stream) {
+  if (!is_q8(dtype & 0xff)) return DA_ERR_DTYPE;
+  if (!k_new || !v_new || !k_new_scale || !v_new_scale) return DA_ERR_NULL;
+  if (seq_lens_out && seq_lens_out == seq_lens) return DA_ERR_SHAPE;
+  if (!aligned16(k_new) || !aligned16(v_new)) return DA_ERR_ALIGN;
+  const QuantArgs qa{k_scale, v_scale, k_new_scale, v_new_scale};
+  return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
+                    num_splits, workspace, workspace_bytes, dev_error, stream, k_new, v_new,
+                    seq_lens_out, &qa);
+}
+
+int kv_quantize(const void* x, int x_dtype, void* codes, float* scales, long long rows, int d,
+                int code_dtype, cudaStream_t stream) {
+  if (!x || !codes || !scales) return DA_ERR_NULL;
+  if ((x_dtype != DA_FP32 && x_dtype != DA_BF16) || !is_q8(code_dtype)) return DA_ERR_DTYPE;
+  if (rows < 0 || d <= 0 || d % 32 != 0 || d > 256 || rows > (1LL << 33)) return DA_ERR_SHAPE;
+  if (rows == 0) return DA_OK;
+  int dev, sms;
+  int st = current_device(&dev, &sms);
+  if (st != DA_OK) return st;
+  cudaError_t e = da::launch_kv_quantize(x, x_dtype == DA_BF16, codes, scales, rows, d,
+                                         code_dtype == DA_INT8 ? 1 : 2, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "kv_quantize launch");
   g_launches.fetch_add(1);
   return DA_OK;
 }

@@ -38,6 +38,13 @@ struct SplitParams {
   void* k_cache;                 // K base (all sequences; b_offset applies)
   void* v_cache;                 // V base
   int32_t* seq_lens_out;         // nullable: receives the lengths after the append
+  // 8-bit caches only: one float32 scale per cached row, [B, h_kv, n_max]
+  // (read through tensor maps; the appended row's scale is written here),
+  // and the scales of the appended rows, [B, h_kv].
+  float* k_scale;
+  float* v_scale;
+  const float* k_new_scale;
+  const float* v_new_scale;
   int append;
   int out_bf16;                  // out holds bf16 (rounded once from the fp32 result)
   int B, h_q, h_kv, group;       // group = h_q / h_kv
@@ -225,6 +232,12 @@ struct KernelShape {
 KernelShape bf16_shape(int d, int group);
 KernelShape f32_shape(int d, int group);
 KernelShape tc5_shape(int group);
+KernelShape q8_shape(int d);
+cudaError_t launch_split_q8(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tks, const CUtensorMap& tvs, int d, int kind,
+                            int grid, cudaStream_t stream);
+cudaError_t launch_kv_quantize(const void* x, int x_bf16, void* codes, float* scales,
+                               long long rows, int d, int kind, cudaStream_t stream);
 cudaError_t launch_split_tc5(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int grid, cudaStream_t stream);
 cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -236,7 +249,8 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const int
                            int max_splits, int n_max, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void* V,
                              const int32_t* pos, int B, int h_kv, int row_bytes_k,
-                             int row_bytes_v, int n_max, int32_t* dev_error, cudaStream_t stream);
+                             int row_bytes_v, int n_max, const float* ks_new, const float* vs_new,
+                             float* ks, float* vs, int32_t* dev_error, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Work list.

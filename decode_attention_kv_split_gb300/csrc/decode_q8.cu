@@ -1,0 +1,531 @@
+// Split-KV decode attention over 8-bit KV caches (sm_103a).
+//
+// A cached row of K (and of V) is d one-byte codes plus one float32 scale;
+// it stands for scale * value(code), value() being the int8 integer or the
+// fp8 e4m3 number.  The page "Attention over the KV cache in the decode step"
+// notes that such a cache halves the bytes streamed per row; the row format
+// is this library's.  Steps I-III of "MoA-Structured Decode Attention"
+// (section 2, eq. 1-3) factor over the row scales:
+//   s[l]      = scale * ks[l] * sum_j q[j] * value(Kc[l][j])
+//   out[h, d] = sum_l a[l] * vs[l] * value(Vc[l][d])
+// so the tensor cores only ever see the codes' values, which fp16 holds
+// exactly (int8: |x| <= 128; e4m3: 3 mantissa bits, exponents 2^-9 .. 2^8),
+// and the scales are applied in fp32 to the scores and to the softmax weights.
+//
+// Structure (as the bf16 kernel): one persistent CTA per SM, a producer warp
+// streaming each item's code tiles and scale tiles with TMA through a ring of
+// stages, consumer warps that each own KBW blocks of 16 rows of a stage.  A
+// consumer warp first converts its own rows' codes into an fp16 tile in
+// shared memory (rows past the end become zeros, an appended row is taken
+// from its slot), reads its rows' scales and releases the stage, then runs
+// the fragment code of the bf16 kernel on fp16 MMAs:
+//   S^T = K_rows . Q^T (mma.m16n8k16, rows of K as M, 8 query heads as N),
+//   online softmax in the log2 domain, P scaled by the V row scales,
+//   O^T += V_rows^T . P^T with P as an fp16 head plus an fp16 remainder.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace da {
+
+namespace q8 {
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> f16x2 (round to nearest even); `lo` lands in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t x) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t x) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
+}
+
+// Four codes (code i in bits 8i..8i+7) -> their exact values as two f16x2
+// words: lo = codes 0, 1; hi = codes 2, 3.
+template <int KIND>
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi);
+
+// int8: the byte x ^ 0x80 = x + 128 placed under the fp16 exponent of 1024
+// gives 1024 + x + 128 exactly; subtracting 1152 leaves x.
+template <>
+__device__ __forceinline__ void codes_to_f16<1>(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x7170);  // bytes u0, 0x64, u1, 0x64
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x7372);  // bytes u2, 0x64, u3, 0x64
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&x);
+  hi = *reinterpret_cast<const uint32_t*>(&y);
+}
+
+// fp8 e4m3: the hardware conversion to f16x2 is exact.
+template <>
+__device__ __forceinline__ void codes_to_f16<2>(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// 2-D tiled TMA load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+}  // namespace q8
+
+template <int D_, int KW_, int KBW_, int STAGES_, int KIND_>
+struct Q8Cfg {
+  static constexpr int D = D_;            // head dim (d_k == d_v)
+  static constexpr int KW = KW_;          // key warps
+  static constexpr int KBW = KBW_;        // 16-row blocks per key warp per stage
+  static constexpr int STAGES = STAGES_;
+  static constexpr int KIND = KIND_;      // 1: int8 codes, 2: fp8 e4m3 codes
+  static constexpr int HG = 1;            // one head group of 8 query heads
+  static constexpr int kHPW = 8;          // heads per warp (one MMA N block)
+  static constexpr int kHeadsPerCta = 8;
+  static constexpr int kTile = 16 * KW * KBW;
+  static constexpr int kConsumerWarps = KW;
+  static constexpr int kConsumerThreads = 32 * KW;
+  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int kCodeBytes = kTile * D;            // one tensor's codes per stage
+  static constexpr int kScaleBytes = kTile * 4;           // one tensor's row scales per stage
+  static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kScaleBytes;
+  static constexpr int kHalfBytes = kTile * 128;          // a 64-column half of an fp16 tile
+  static constexpr int kF16TileBytes = kTile * D * 2;     // one tensor, fp16
+  static constexpr int kQBytes = kHeadsPerCta * D * 2;    // bf16 q rows of one item, per stage
+  static constexpr int kNewBytes = 2 * D;                 // appended K and V code rows, per stage
+  static constexpr int kSlotStride = D + 4;
+  static constexpr int kEpiAccFloats = KW * kHPW * kSlotStride;
+  static constexpr int kEpiMLFloats = 2 * KW * kHPW;
+  static constexpr int kSchedWords = da::kSchedWords;
+  static constexpr size_t kSmemBytes =
+      1024 + size_t(STAGES) * (kStageBytes + kQBytes + kNewBytes) + 2 * size_t(kF16TileBytes) +
+      size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 + 2 * STAGES * 8 + 16;
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(KIND == 1 || KIND == 2, "code type");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert((kEpiAccFloats + kEpiMLFloats) % 2 == 0, "mbarrier alignment");
+};
+
+// Byte offset of column `col` (a multiple of 8) of row `row` of an fp16
+// tile: 64-column halves of 128-byte rows, 128-byte swizzle.
+template <class Cfg>
+__device__ __forceinline__ uint32_t swz_f16(int row, int col) {
+  const int half = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return uint32_t(half * Cfg::kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Producer: one thread streams every stage of the CTA's items: the K and V
+// code tiles and row scales, the item's bf16 q rows on its first stage, and
+// the appended code rows on the stage that holds them.
+template <class Cfg>
+__device__ __forceinline__ void produce_q8(const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                           const CUtensorMap* tmKs, const CUtensorMap* tmVs,
+                                           const SplitParams& p, const Schedule& s, uint32_t ring,
+                                           uint32_t qslots, uint32_t newslots, uint32_t full0,
+                                           uint32_t empty0, volatile int* abort_flag) {
+  constexpr int T = Cfg::kTile, STAGES = Cfg::STAGES, D = Cfg::D;
+  const uint64_t policy = l2_policy_evict_first();
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, issued_parity = 0;
+  bool aborted = false;
+  for (int i = blockIdx.x, k = 0; i < s.total && !aborted; i += gridDim.x, ++k) {
+    const Item it = cta_item<T>(p, s, i, k);
+    const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
+    for (int t = 0; t < it.tiles; ++t) {
+      if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+        *abort_flag = 1;
+        flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      const uint32_t bar = full0 + 8 * stage;
+      const int y0 = it.row_begin + t * T;
+      const bool with_new = it.new_row >= y0 && it.new_row < y0 + T;
+      uint32_t extra = 0;
+      const int h0 = it.hc * Cfg::kHeadsPerCta;
+      const int nh = min(Cfg::kHeadsPerCta, p.group - h0);
+      if (t == 0) extra += uint32_t(nh) * (D * 2);
+      if (with_new) extra += 2 * D;
+      mbar_arrive_expect_tx(bar, Cfg::kStageBytes + extra);
+      if (t == 0) {
+        const char* qsrc = static_cast<const char*>(p.q) +
+                           (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * (D * 2);
+        bulk_load(qslots + stage * Cfg::kQBytes, qsrc, uint32_t(nh) * (D * 2), bar);
+      }
+      if (with_new) {
+        const size_t src = (size_t(it.b) * p.h_kv + it.kvh) * D;
+        bulk_load(newslots + stage * Cfg::kNewBytes, static_cast<const char*>(p.k_new) + src, D,
+                  bar);
+        bulk_load(newslots + stage * Cfg::kNewBytes + D, static_cast<const char*>(p.v_new) + src,
+                  D, bar);
+      }
+      const uint32_t dst = ring + stage * Cfg::kStageBytes;
+      tma_load_3d(dst, tmK, 0, y0, z, bar, policy);
+      tma_load_3d(dst + Cfg::kCodeBytes, tmV, 0, y0, z, bar, policy);
+      q8::tma_load_2d(dst + 2 * Cfg::kCodeBytes, tmKs, y0, z, bar, policy);
+      q8::tma_load_2d(dst + 2 * Cfg::kCodeBytes + Cfg::kScaleBytes, tmVs, y0, z, bar, policy);
+      issued |= 1u << stage;
+      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (aborted) {
+    volatile int never = 0;
+    for (int st = 0; st < STAGES; ++st)
+      if (issued & (1u << st)) mbar_wait_bounded(full0 + 8 * st, (issued_parity >> st) & 1u, &never);
+  }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    split_decode_q8_kernel(const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV,
+                           const __grid_constant__ CUtensorMap tmKs,
+                           const __grid_constant__ CUtensorMap tmVs, const SplitParams p) {
+  constexpr int D = Cfg::D, KW = Cfg::KW, KBW = Cfg::KBW, STAGES = Cfg::STAGES, T = Cfg::kTile;
+  constexpr int kHPW = Cfg::kHPW;
+  constexpr int MB = D / 16;       // 16-wide blocks of d
+  constexpr int RW = KBW * 16;     // rows owned by one consumer warp
+  constexpr int CPR = D / 16;      // 16-code chunks per row
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* kf16 = smem + size_t(STAGES) * Cfg::kStageBytes;  // fp16 K tile (1024-aligned)
+  uint8_t* vf16 = kf16 + Cfg::kF16TileBytes;                 // fp16 V tile
+  uint8_t* qslots = vf16 + Cfg::kF16TileBytes;
+  uint8_t* newslots = qslots + size_t(STAGES) * Cfg::kQBytes;
+  float* epi_acc = reinterpret_cast<float*>(newslots + size_t(STAGES) * Cfg::kNewBytes);
+  float* epi_m = epi_acc + Cfg::kEpiAccFloats;
+  float* epi_l = epi_m + KW * kHPW;
+  int* sched_words = reinterpret_cast<int*>(epi_l + KW * kHPW);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sched_words + Cfg::kSchedWords);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {  // the tensor maps do not depend on the preceding grid
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmKs);
+    prefetch_tmap(&tmVs);
+  }
+  // Launched as a programmatic dependent: nothing before this line reads
+  // memory that the previous grid on the stream may write.
+  wait_for_prerequisite_grid();
+  const Schedule sched = build_schedule<T>(p, sched_words);
+  allow_dependent_launch();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == KW) {
+    if (lane == 0)
+      produce_q8<Cfg>(&tmK, &tmV, &tmKs, &tmVs, p, sched, ring, smem_u32(qslots),
+                      smem_u32(newslots), full0, empty0, abort_flag);
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int kw = warp;
+  const int r = lane >> 2;  // MMA fragment row group
+  const int c = lane & 3;   // MMA fragment column pair
+  const int key0 = kw * RW;  // first row of this warp inside a stage
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
+    const Item it = cta_item<T>(p, sched, i, k);
+    const int head_base = it.hc * Cfg::kHeadsPerCta;
+    const size_t kvhead = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
+    uint32_t qf[MB][2];
+
+    float m_run[2], l_run[2];
+    float acc[MB][4];
+    m_run[0] = m_run[1] = -INFINITY;
+    l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mb][e] = 0.f;
+
+    for (int t = 0; t < it.tiles; ++t) {
+      if (!mbar_wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
+        if (!*abort_flag) {
+          *abort_flag = 1;
+          flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
+        }
+      }
+      const uint8_t* st = smem + size_t(stage) * Cfg::kStageBytes;
+      const float* ks_t = reinterpret_cast<const float*>(st + 2 * Cfg::kCodeBytes);
+      const float* vs_t = ks_t + T;
+      const uint8_t* nslot = newslots + size_t(stage) * Cfg::kNewBytes;
+      const int tile_row0 = it.row_begin + t * T;
+      const int valid = min(T, it.row_end - tile_row0);
+      const int new_local = (it.new_row >= tile_row0 && it.new_row < tile_row0 + T)
+                                ? it.new_row - tile_row0
+                                : -1;
+      const bool mine_new = new_local >= key0 && new_local < key0 + RW;
+
+      // ---- this warp's rows: codes -> fp16 tiles (zeros past the end)
+#pragma unroll 4
+      for (int ch = lane; ch < 2 * RW * CPR; ch += 32) {
+        const int tensor = ch / (RW * CPR);  // 0: K, 1: V
+        const int rc = ch - tensor * RW * CPR;
+        const int row = key0 + rc / CPR;
+        const int col = (rc % CPR) * 16;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (row < valid) {
+          const uint8_t* src = row == new_local ? nslot + tensor * D + col
+                                                : st + tensor * Cfg::kCodeBytes + row * D + col;
+          w = *reinterpret_cast<const uint4*>(src);
+        }
+        uint4 a, b;
+        q8::codes_to_f16<Cfg::KIND>(w.x, a.x, a.y);
+        q8::codes_to_f16<Cfg::KIND>(w.y, a.z, a.w);
+        q8::codes_to_f16<Cfg::KIND>(w.z, b.x, b.y);
+        q8::codes_to_f16<Cfg::KIND>(w.w, b.z, b.w);
+        if (row >= valid) a = b = make_uint4(0, 0, 0, 0);
+        uint8_t* dst = tensor ? vf16 : kf16;
+        *reinterpret_cast<uint4*>(dst + swz_f16<Cfg>(row, col)) = a;
+        *reinterpret_cast<uint4*>(dst + swz_f16<Cfg>(row, col + 8)) = b;
+      }
+      // ---- this lane's row scales (0 past the end; the appended row's own)
+      float fk[KBW][2], fv[KBW][2];
+#pragma unroll
+      for (int kb = 0; kb < KBW; ++kb)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = key0 + kb * 16 + r + 8 * hh;
+          float sk = ks_t[row], sv = vs_t[row];
+          if (row == new_local) {
+            sk = __ldg(p.k_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+            sv = __ldg(p.v_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+          }
+          fk[kb][hh] = row < valid ? sk * p.scale_log2 : 0.f;
+          fv[kb][hh] = row < valid ? sv : 0.f;
+        }
+      if (t == 0) {  // q rows of the item's heads, bf16 -> fp16 fragments
+        const uint32_t* qs =
+            reinterpret_cast<const uint32_t*>(qslots + size_t(stage) * Cfg::kQBytes);
+        const bool ok = head_base + r < p.group;
+#pragma unroll
+        for (int ks = 0; ks < MB; ++ks) {
+          const uint32_t a0 = ok ? qs[r * (D / 2) + ks * 8 + c] : 0u;
+          const uint32_t a1 = ok ? qs[r * (D / 2) + ks * 8 + 4 + c] : 0u;
+          qf[ks][0] = q8::pack_f16x2(bf16_lo_to_f32(a0), bf16_hi_to_f32(a0));
+          qf[ks][1] = q8::pack_f16x2(bf16_lo_to_f32(a1), bf16_hi_to_f32(a1));
+        }
+      }
+      // the appended row goes into the caches once per kv head, by the warp that owns it
+      if (mine_new && it.hc == 0 && !*abort_flag) {
+        const size_t row_off = kvhead * size_t(p.n_max) + size_t(it.new_row);
+        if (lane < D / 16) {
+          reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + row_off * D)[lane] =
+              reinterpret_cast<const uint4*>(nslot)[lane];
+          reinterpret_cast<uint4*>(static_cast<char*>(p.v_cache) + row_off * D)[lane] =
+              reinterpret_cast<const uint4*>(nslot + D)[lane];
+        }
+        if (lane == 0) {
+          p.k_scale[row_off] = __ldg(p.k_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+          p.v_scale[row_off] = __ldg(p.v_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+        }
+      }
+      __syncwarp();
+      // the stage's codes, scales and q are all in registers or the fp16 tiles now
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+
+      if (!*abort_flag && key0 < valid) {
+        const uint32_t kbase = smem_u32(kf16);
+        const uint32_t vbase = smem_u32(vf16);
+        // ---- Step I: scores for KBW blocks of 16 rows
+        float s[KBW][4];
+#pragma unroll
+        for (int kb = 0; kb < KBW; ++kb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[kb][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < MB; ++ks) {
+#pragma unroll
+          for (int kb = 0; kb < KBW; ++kb) {
+            const int row = key0 + kb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int col = ks * 16 + (lane >> 4) * 8;
+            uint32_t a[4];
+            ldmatrix_x4(a, kbase + swz_f16<Cfg>(row, col));
+            q8::mma_f16_16816(s[kb], a, qf[ks][0], qf[ks][1]);
+          }
+        }
+        // ---- Step II: scale by the K row scales, mask, running max and sum
+        float alpha[2];
+        bool changed = false;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int kb = 0; kb < KBW; ++kb) {
+            const int row_lo = key0 + kb * 16 + r;
+            s[kb][j] = row_lo < valid ? s[kb][j] * fk[kb][0] : -INFINITY;
+            s[kb][j + 2] = row_lo + 8 < valid ? s[kb][j + 2] * fk[kb][1] : -INFINITY;
+            mx = fmaxf(mx, fmaxf(s[kb][j], s[kb][j + 2]));
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[j], mx);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha[j] = ex2(m_run[j] - m_use);
+          changed |= (m_new != m_run[j]);
+          m_run[j] = m_new;
+          float sum = 0.f;
+#pragma unroll
+          for (int kb = 0; kb < KBW; ++kb) {
+            s[kb][j] = ex2(s[kb][j] - m_use);
+            s[kb][j + 2] = ex2(s[kb][j + 2] - m_use);
+            sum += s[kb][j] + s[kb][j + 2];
+          }
+          l_run[j] = l_run[j] * alpha[j] + sum;
+        }
+        if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) {
+            acc[mb][0] *= alpha[0];
+            acc[mb][1] *= alpha[1];
+            acc[mb][2] *= alpha[0];
+            acc[mb][3] *= alpha[1];
+          }
+        }
+        // ---- Step III: O^T += V^T . (P * vs)^T, P as fp16 head + fp16 remainder
+#pragma unroll
+        for (int kb = 0; kb < KBW; ++kb) {
+          const float p0 = s[kb][0] * fv[kb][0], p1 = s[kb][1] * fv[kb][0];
+          const float p2 = s[kb][2] * fv[kb][1], p3 = s[kb][3] * fv[kb][1];
+          const uint32_t h0 = q8::pack_f16x2(p0, p1);  // row r
+          const uint32_t h1 = q8::pack_f16x2(p2, p3);  // row r + 8
+          const uint32_t l0 = q8::pack_f16x2(p0 - q8::f16_lo(h0), p1 - q8::f16_hi(h0));
+          const uint32_t l1 = q8::pack_f16x2(p2 - q8::f16_lo(h1), p3 - q8::f16_hi(h1));
+          const uint32_t ph0 = movmatrix_trans(h0), ph1 = movmatrix_trans(h1);
+          const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
+          const int blk0 = key0 + kb * 16;
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) {
+            const int row = blk0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+            const int col = mb * 16 + ((lane >> 3) & 1) * 8;
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, vbase + swz_f16<Cfg>(row, col));
+            q8::mma_f16_16816(acc[mb], a, ph0, ph1);
+            q8::mma_f16_16816(acc[mb], a, pl0, pl1);
+          }
+        }
+      }
+      __syncwarp();  // the fp16 tiles are rewritten for the next stage
+    }
+
+    // ---- Epilogue: per-warp state to shared slots, then the shared finish.
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = l_run[j];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l_run[j] = v;
+    }
+    named_bar_sync(1, Cfg::kConsumerThreads);  // earlier readers of the slots are done
+    float* slot = epi_acc + kw * kHPW * Cfg::kSlotStride;
+    if (lane < 4) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        epi_m[kw * kHPW + 2 * lane + j] = m_run[j];
+        epi_l[kw * kHPW + 2 * lane + j] = l_run[j];
+      }
+    }
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+      const int d0 = mb * 16 + r;
+      const int h0 = 2 * c;
+      slot[h0 * Cfg::kSlotStride + d0] = acc[mb][0];
+      slot[(h0 + 1) * Cfg::kSlotStride + d0] = acc[mb][1];
+      slot[h0 * Cfg::kSlotStride + d0 + 8] = acc[mb][2];
+      slot[(h0 + 1) * Cfg::kSlotStride + d0 + 8] = acc[mb][3];
+    }
+    named_bar_sync(1, Cfg::kConsumerThreads);
+    finish_item<D, 1, KW, kHPW, Cfg::kSlotStride>(p, it, epi_acc, epi_m, epi_l, threadIdx.x,
+                                                  Cfg::kConsumerThreads, abort_flag);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Variants and launcher.
+// ---------------------------------------------------------------------------
+template <int KIND>
+using Q8D128 = Q8Cfg<128, 4, 2, 3, KIND>;
+template <int KIND>
+using Q8D64 = Q8Cfg<64, 4, 2, 6, KIND>;
+
+KernelShape q8_shape(int d) {
+  const int tile = d == 128 ? Q8D128<1>::kTile : Q8D64<1>::kTile;
+  return KernelShape{tile, 8, d, 0, 1.0f};
+}
+
+template <class Cfg>
+static cudaError_t launch_q8_cfg(const SplitParams& p, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tks,
+                                 const CUtensorMap& tvs, int grid, cudaStream_t stream) {
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(split_decode_q8_kernel<Cfg>, Cfg::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(split_decode_q8_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes,
+                          stream, tk, tv, tks, tvs, p);
+}
+
+cudaError_t launch_split_q8(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tks, const CUtensorMap& tvs, int d, int kind,
+                            int grid, cudaStream_t stream) {
+  if (d == 128)
+    return kind == 1 ? launch_q8_cfg<Q8D128<1>>(p, tk, tv, tks, tvs, grid, stream)
+                     : launch_q8_cfg<Q8D128<2>>(p, tk, tv, tks, tvs, grid, stream);
+  return kind == 1 ? launch_q8_cfg<Q8D64<1>>(p, tk, tv, tks, tvs, grid, stream)
+                   : launch_q8_cfg<Q8D64<2>>(p, tk, tv, tks, tvs, grid, stream);
+}
+
+}  // namespace da

@@ -47,10 +47,16 @@ extern "C" {
 #define DA_API
 #endif
 
-/* Element type of q, K, V (and of the rows appended by kv_append). */
+/*
+ * Element type of q, K, V (and of the rows appended by kv_append).  DA_INT8
+ * and DA_FP8_E4M3 are 8-bit caches (the *_q8 entry points only): K and V
+ * hold one-byte codes, each cached row has one float32 scale, q is bf16.
+ */
 typedef enum {
   DA_FP32 = 0,
-  DA_BF16 = 1
+  DA_BF16 = 1,
+  DA_INT8 = 2,
+  DA_FP8_E4M3 = 3
 } da_dtype;
 
 typedef enum {
@@ -212,6 +218,65 @@ DA_API int decode_attn_noalloc(const void* q, const void* K, const void* V, cons
 DA_API int kv_append(const void* k_new, const void* v_new, void* K, void* V, const int32_t* pos,
                      int B, int h_kv, int d_k, int d_v, int n_max, int dtype,
                      int32_t* dev_error, cudaStream_t stream);
+
+/*
+ * 8-bit KV caches ("Attention over the KV cache in the decode step" notes
+ * that an int8 or fp8 cache halves the bytes per cached row and doubles the
+ * arithmetic intensity; the pages fix no format, so this one is the
+ * library's).  A cached row of K (or V) is d one-byte codes c[j] plus one
+ * float32 scale s, and stands for s * value(c[j]):
+ *   DA_INT8      value = the two's-complement integer (-128 .. 127)
+ *   DA_FP8_E4M3  value = the fp8 e4m3 number (bias 7, 3 mantissa bits,
+ *                subnormals below 2^-6, S.1111.111 the only NaN, max 448)
+ * Layouts (row-major, device):
+ *   K, V            [B, h_kv, n_max, d]  codes (1 byte each)
+ *   k_scale, v_scale [B, h_kv, n_max]    float32, one per cached row,
+ *                                        16-byte aligned
+ *   q               [B, h_q, d]          bfloat16
+ *   out             as decode_attn_ex (float32, or bf16 with DA_OUT_BF16)
+ * The decode computes Steps I-III of decode_attn_ex on the values the codes
+ * and scales stand for; fp16 tensor cores see the codes' exact values, the
+ * scales are applied in float32.  Row scales must be finite and below 65504
+ * in magnitude; rows at or beyond seq_lens[b] may hold anything.  Extra
+ * requirements: n_max a multiple of 4; d_k == d_v in {64, 128}.
+ */
+
+/* Decode over an 8-bit cache; arguments as decode_attn_ex plus the row
+ * scales.  dtype is DA_INT8 or DA_FP8_E4M3 (| DA_OUT_BF16); the workspace
+ * size is decode_attn_workspace_bytes of the same dtype. */
+DA_API int decode_attn_q8_ex(const void* q, const void* K, const void* V, const float* k_scale,
+                             const float* v_scale, const int32_t* seq_lens, void* out, int B,
+                             int h_q, int h_kv, int d_k, int d_v, int n_max, float scale,
+                             int dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_error, cudaStream_t stream);
+
+/* decode_attn_append for an 8-bit cache: the new rows arrive as codes
+ * k_new/v_new [B, h_kv, d] (1 byte each, 16-byte aligned) with their scales
+ * k_new_scale/v_new_scale [B, h_kv] (float32); codes and scale are copied
+ * into row seq_lens[b] of the caches and take part in the same decode. */
+DA_API int decode_attn_q8_append(const void* q, const void* k_new, const void* v_new,
+                                 const float* k_new_scale, const float* v_new_scale, void* K,
+                                 void* V, float* k_scale, float* v_scale, const int32_t* seq_lens,
+                                 int32_t* seq_lens_out, void* out, int B, int h_q, int h_kv,
+                                 int d_k, int d_v, int n_max, float scale, int dtype,
+                                 int num_splits, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_error, cudaStream_t stream);
+
+/* kv_append for an 8-bit cache: row pos[b] of every kv head receives the
+ * code rows k_new/v_new [B, h_kv, d] and the scales k_new_scale/v_new_scale
+ * [B, h_kv], bit for bit; errors as kv_append. */
+DA_API int kv_append_q8(const void* k_new, const void* v_new, const float* k_new_scale,
+                        const float* v_new_scale, void* K, void* V, float* k_scale,
+                        float* v_scale, const int32_t* pos, int B, int h_kv, int d_k, int d_v,
+                        int n_max, int dtype, int32_t* dev_error, cudaStream_t stream);
+
+/* Quantize rows x [rows, d] (x_dtype DA_FP32 or DA_BF16, device) into codes
+ * [rows, d] (code_dtype DA_INT8 or DA_FP8_E4M3) and scales [rows] (float32):
+ * a = max_j |x[j]|, s = a / Q (Q = 127 or 448, float32 division),
+ * code[j] = round-to-nearest-even(x[j] / s) clamped to [-Q, Q], all codes 0
+ * when s = 0.  x must be finite; d a multiple of 32, at most 256. */
+DA_API int kv_quantize(const void* x, int x_dtype, void* codes, float* scales, long long rows,
+                       int d, int code_dtype, cudaStream_t stream);
 
 /* Static, human-readable name of a da_status. */
 DA_API const char* decode_attn_status_string(int status);

@@ -278,22 +278,35 @@ class Harness:
                       num_splits=w.num_splits, description=w.description)
         seed = 1000 * rank
         lens0 = W.seq_lens(wb, seed)
-        es = 2 if w.dtype == torch.bfloat16 else 4
-        kv_touch = accounting.decode_bytes((lens0 + CYCLE).tolist(), w.h_q, w.h_kv, w.d_k, w.d_v,
-                                           es)
+        self.q8 = W.is_q8(w)
+        es = 1 if self.q8 else (2 if w.dtype == torch.bfloat16 else 4)
+        row_bytes = (w.d_k + 4) if self.q8 else w.d_k * es  # an 8-bit row carries its scale
+        self.w, self.es = w, es
+        kv_touch = self._decode_bytes((lens0 + CYCLE).tolist())
         n_rot = max(1, math.ceil(4 * L2_BYTES / kv_touch))
-        cache_bytes = 2 * wb.B * wb.h_kv * n_max * wb.d_k * es
+        cache_bytes = 2 * wb.B * wb.h_kv * n_max * row_bytes
         free = torch.cuda.mem_get_info(dev)[0]
         n_rot = int(max(1, min(n_rot, 64, (0.6 * free) // cache_bytes)))
 
         K0, V0 = W.cache(wb, seed, device=dev if gpu_cache else "cpu")
         K0, V0 = K0.to(dev), V0.to(dev)
-        self.caches = [(K0, V0)] + [(K0.clone(), V0.clone()) for _ in range(n_rot - 1)]
-        del K0, V0
+        if self.q8:  # 8-bit cache: codes + row scales, quantized by the library's kernel
+            (K0, ks0), (V0, vs0) = api.kv_quantize(K0, w.dtype), api.kv_quantize(V0, w.dtype)
+            first = (K0, V0, ks0, vs0)
+        else:
+            first = (K0, V0)
+        self.caches = [first] + [tuple(t.clone() for t in first) for _ in range(n_rot - 1)]
+        del K0, V0, first
         self.q = W.query(wb, seed).to(dev)
         rows = [W.new_rows(wb, t, seed) for t in range(CYCLE)]
-        self.k_new = [k.to(dev) for k, _ in rows]
-        self.v_new = [v.to(dev) for _, v in rows]
+        if self.q8:
+            kq = [api.kv_quantize(k.to(dev), w.dtype) for k, _ in rows]
+            vq = [api.kv_quantize(v.to(dev), w.dtype) for _, v in rows]
+            self.k_new, self.k_new_scale = [c for c, _ in kq], [s for _, s in kq]
+            self.v_new, self.v_new_scale = [c for c, _ in vq], [s for _, s in vq]
+        else:
+            self.k_new = [k.to(dev) for k, _ in rows]
+            self.v_new = [v.to(dev) for _, v in rows]
         self.pos_t = [(lens0 + t).to(torch.int32).to(dev) for t in range(CYCLE)]
         self.lens_t = [(lens0 + t + 1).to(torch.int32).to(dev) for t in range(CYCLE)]
         self.out = torch.empty((wb.B, wb.h_q, wb.d_v), dtype=torch.float32, device=dev)
@@ -303,17 +316,35 @@ class Harness:
                                        w.num_splits)
         self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream(dev)
-        self.w, self.wb, self.lens0, self.es = w, wb, lens0, es
+        self.wb, self.lens0 = wb, lens0
         self.n_rot, self.kv_touch, self.fused = n_rot, kv_touch, fused
 
-    def step(self, i, qq=None, kn=None, vn=None):
+    def _decode_bytes(self, lens) -> int:
+        w = self.w
+        if self.q8:
+            return accounting.decode_bytes_q8(lens, w.h_q, w.h_kv, w.d_k, w.d_v)
+        return accounting.decode_bytes(lens, w.h_q, w.h_kv, w.d_k, w.d_v, self.es)
+
+    def step(self, i, qq=None, kn=None, vn=None, kns=None, vns=None):
         """One pass of the hot path: append row pos of every kv head, decode over pos+1."""
         api, w = self.api, self.w
-        K, V = self.caches[i % self.n_rot]
         c = i % CYCLE
         qq = self.q if qq is None else qq
         kn = self.k_new[c] if kn is None else kn
         vn = self.v_new[c] if vn is None else vn
+        if self.q8:
+            K, V, ks, vs = self.caches[i % self.n_rot]
+            kns = self.k_new_scale[c] if kns is None else kns
+            vns = self.v_new_scale[c] if vns is None else vns
+            if self.fused:
+                api.decode_attn_q8_append(qq, kn, vn, kns, vns, K, V, ks, vs, self.pos_t[c],
+                                          out=self.out, num_splits=w.num_splits, workspace=self.ws)
+            else:
+                api.kv_append_q8(kn, vn, kns, vns, K, V, ks, vs, self.pos_t[c])
+                api.decode_attn_q8(qq, K, V, ks, vs, self.lens_t[c], out=self.out,
+                                   num_splits=w.num_splits, workspace=self.ws)
+            return
+        K, V = self.caches[i % self.n_rot]
         if self.fused:
             api.decode_attn_append(qq, kn, vn, K, V, self.pos_t[c], out=self.out,
                                    num_splits=w.num_splits, workspace=self.ws)
@@ -326,8 +357,9 @@ class Harness:
         """Algorithmic HBM bytes of one step at the mean context of the 16-step cycle."""
         w = self.w
         mean_lens = [int(n) + (CYCLE + 1) / 2 for n in self.lens0.tolist()]
-        dec = accounting.decode_bytes(mean_lens, w.h_q, w.h_kv, w.d_k, w.d_v, self.es)
-        app = accounting.append_bytes(w.B, w.h_kv, w.d_k, w.d_v, self.es)
+        dec = self._decode_bytes(mean_lens)
+        app = (accounting.append_bytes_q8(w.B, w.h_kv, w.d_k, w.d_v) if self.q8
+               else accounting.append_bytes(w.B, w.h_kv, w.d_k, w.d_v, self.es))
         # the fused call reads the new row once (from k_new/v_new) and writes it once
         return dec + app // 2 if self.fused else dec + app
 
@@ -398,34 +430,32 @@ def run_ours(args, w, world, rank, local):
     clocks = sampler.stop() if sampler else None
 
     # ---- end to end: pinned host inputs in, result out, every step
+    # per step: q and the new rows (with their scales for an 8-bit cache)
+    rows_d = [k_new, v_new] + ([h.k_new_scale, h.v_new_scale] if h.q8 else [])
+    rows_h = [[t.cpu().pin_memory() for t in ts] for ts in rows_d]
     q_h = q.cpu().pin_memory()
-    kn_h = [k.cpu().pin_memory() for k in k_new]
-    vn_h = [v.cpu().pin_memory() for v in v_new]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     q_d = torch.empty_like(q)
-    kn_d = torch.empty_like(k_new[0])
-    vn_d = torch.empty_like(v_new[0])
-    e2e_steps = max(1, min(K, 2000))
-    for i in range(min(args.warmup, 8)):
+    bufs = [torch.empty_like(ts[0]) for ts in rows_d]
+
+    def e2e_step(i):
         c = i % CYCLE
         q_d.copy_(q_h, non_blocking=True)
-        kn_d.copy_(kn_h[c], non_blocking=True)
-        vn_d.copy_(vn_h[c], non_blocking=True)
-        step(i, q_d, kn_d, vn_d)
+        for b, hs in zip(bufs, rows_h):
+            b.copy_(hs[c], non_blocking=True)
+        step(i, q_d, *bufs)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
+
+    e2e_steps = max(1, min(K, 2000))
+    for i in range(min(args.warmup, 8)):
+        e2e_step(i)
     barrier(world)
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        c = i % CYCLE
-        q_d.copy_(q_h, non_blocking=True)
-        kn_d.copy_(kn_h[c], non_blocking=True)
-        vn_d.copy_(vn_h[c], non_blocking=True)
-        step(i, q_d, kn_d, vn_d)
-        out_h.copy_(out, non_blocking=True)
-        stream.synchronize()
+        e2e_step(i)
     _, e2e_rate = replica_rate(1e3 * (time.perf_counter() - t0), world, w.B, e2e_steps)
-    h2d = q.numel() * q.element_size() + 2 * k_new[0].numel() * k_new[0].element_size()
+    h2d = q.numel() * q.element_size() + sum(b.numel() * b.element_size() for b in bufs)
     d2h = out.numel() * out.element_size()
 
     if rank != 0:
@@ -444,7 +474,8 @@ def run_ours(args, w, world, rank, local):
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if w.dtype == torch.float32 else "bf16",
+        "dtype": ("f16 (8-bit codes, fp32 scales)" if h.q8
+                  else "f32" if w.dtype == torch.float32 else "bf16"),
         "data": "synthetic", "config": workload_config(wb, n_rot, kv_touch),
         "hbm_gbs": achieved,
         "hbm_frac_of_8tbs": achieved / 8000.0,

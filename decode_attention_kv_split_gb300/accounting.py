@@ -35,6 +35,21 @@ def append_bytes(B: int, h_kv: int, d_k: int, d_v: int, elem_bytes: int) -> int:
     return 2 * B * h_kv * (d_k + d_v) * elem_bytes
 
 
+def decode_bytes_q8(seq_lens: Sequence[int], h_q: int, h_kv: int, d_k: int, d_v: int,
+                    out_bytes: int = 4) -> int:
+    """decode_bytes for an 8-bit cache: every cached K and V row is one byte per
+    element plus one float32 scale; q is bf16."""
+    rows = sum(n for n in seq_lens)
+    B = len(seq_lens)
+    kv = rows * h_kv * (d_k + 4 + d_v + 4)
+    return int(kv + B * h_q * d_k * 2 + B * h_q * d_v * out_bytes)
+
+
+def append_bytes_q8(B: int, h_kv: int, d_k: int, d_v: int) -> int:
+    """append_bytes for an 8-bit cache: code rows and their scales, read once and written once."""
+    return 2 * B * h_kv * (d_k + 4 + d_v + 4)
+
+
 def decode_flops(seq_lens: Sequence[int], h_q: int, d_k: int, d_v: int) -> int:
     """Multiply-adds x 2 for q.K over every row and p.V over every row."""
     rows = sum(int(n) for n in seq_lens)

@@ -271,6 +271,34 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
 
+  // Which 16-code chunks of its rows a lane converts: chunk u of lane L is
+  // number L + 32 u of the warp's 2 * RW * CPR chunks (K rows, then V rows).
+  // For d = 128 a quarter-warp covers two rows in opposite 64-column halves,
+  // so neither the 16-byte code reads nor the swizzled fp16 writes share a
+  // bank; for d = 64 (64-byte rows) it covers two whole rows.  Everything but
+  // the stage base is fixed per lane.
+  constexpr int kChunks = 2 * RW * CPR / 32;
+  static_assert((RW * CPR) % 32 == 0, "chunks split evenly between K and V");
+  int lane_row, chunk_col;
+  if (D == 128) {
+    const int qa = (lane >> 3) & 1, sub = lane & 7, r2 = sub >> 2;
+    lane_row = 2 * (lane >> 4) + r2;   // rows step by 4 per 32 chunks
+    chunk_col = (r2 ^ qa) * 64 + (sub & 3) * 16;
+  } else {
+    lane_row = lane >> 2;              // rows step by 8 per 32 chunks
+    chunk_col = (lane & 3) * 16;
+  }
+  constexpr int kRowStep = 32 / CPR;   // rows advanced by 32 chunks
+  auto chunk_tensor = [&](int u) { return u / (kChunks / 2); };
+  auto chunk_row = [&](int u) { return key0 + lane_row + (u % (kChunks / 2)) * kRowStep; };
+  const int src_off0 = (key0 + lane_row) * D + chunk_col;
+  auto chunk_src = [&](int u) {
+    return chunk_tensor(u) * Cfg::kCodeBytes + (u % (kChunks / 2)) * kRowStep * D;
+  };
+  auto chunk_dst = [&](int u, int c8) {
+    return chunk_tensor(u) * Cfg::kF16TileBytes + int(swz_f16<Cfg>(chunk_row(u), chunk_col + c8));
+  };
+
   for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
     const Item it = cta_item<T>(p, sched, i, k);
     const int head_base = it.hc * Cfg::kHeadsPerCta;
@@ -305,27 +333,37 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const bool mine_new = new_local >= key0 && new_local < key0 + RW;
 
       // ---- this warp's rows: codes -> fp16 tiles (zeros past the end)
-#pragma unroll 4
-      for (int ch = lane; ch < 2 * RW * CPR; ch += 32) {
-        const int tensor = ch / (RW * CPR);  // 0: K, 1: V
-        const int rc = ch - tensor * RW * CPR;
-        const int row = key0 + rc / CPR;
-        const int col = (rc % CPR) * 16;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (row < valid) {
-          const uint8_t* src = row == new_local ? nslot + tensor * D + col
-                                                : st + tensor * Cfg::kCodeBytes + row * D + col;
-          w = *reinterpret_cast<const uint4*>(src);
+      if (valid == T && new_local < 0) {  // a full tile with no appended row (warp-uniform)
+#pragma unroll
+        for (int u = 0; u < kChunks; ++u) {
+          const uint4 w = *reinterpret_cast<const uint4*>(st + src_off0 + chunk_src(u));
+          uint4 a, b;
+          q8::codes_to_f16<Cfg::KIND>(w.x, a.x, a.y);
+          q8::codes_to_f16<Cfg::KIND>(w.y, a.z, a.w);
+          q8::codes_to_f16<Cfg::KIND>(w.z, b.x, b.y);
+          q8::codes_to_f16<Cfg::KIND>(w.w, b.z, b.w);
+          *reinterpret_cast<uint4*>(kf16 + chunk_dst(u, 0)) = a;
+          *reinterpret_cast<uint4*>(kf16 + chunk_dst(u, 8)) = b;
         }
-        uint4 a, b;
-        q8::codes_to_f16<Cfg::KIND>(w.x, a.x, a.y);
-        q8::codes_to_f16<Cfg::KIND>(w.y, a.z, a.w);
-        q8::codes_to_f16<Cfg::KIND>(w.z, b.x, b.y);
-        q8::codes_to_f16<Cfg::KIND>(w.w, b.z, b.w);
-        if (row >= valid) a = b = make_uint4(0, 0, 0, 0);
-        uint8_t* dst = tensor ? vf16 : kf16;
-        *reinterpret_cast<uint4*>(dst + swz_f16<Cfg>(row, col)) = a;
-        *reinterpret_cast<uint4*>(dst + swz_f16<Cfg>(row, col + 8)) = b;
+      } else {
+#pragma unroll 2
+        for (int u = 0; u < kChunks; ++u) {
+          const int tensor = chunk_tensor(u), row = chunk_row(u), col = chunk_col;
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (row < valid) {
+            const uint8_t* src = row == new_local ? nslot + tensor * D + col
+                                                  : st + src_off0 + chunk_src(u);
+            w = *reinterpret_cast<const uint4*>(src);
+          }
+          uint4 a, b;
+          q8::codes_to_f16<Cfg::KIND>(w.x, a.x, a.y);
+          q8::codes_to_f16<Cfg::KIND>(w.y, a.z, a.w);
+          q8::codes_to_f16<Cfg::KIND>(w.z, b.x, b.y);
+          q8::codes_to_f16<Cfg::KIND>(w.w, b.z, b.w);
+          if (row >= valid) a = b = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(kf16 + chunk_dst(u, 0)) = a;
+          *reinterpret_cast<uint4*>(kf16 + chunk_dst(u, 8)) = b;
+        }
       }
       // ---- this lane's row scales (0 past the end; the appended row's own)
       float fk[KBW][2], fv[KBW][2];
@@ -498,9 +536,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 // Variants and launcher.
 // ---------------------------------------------------------------------------
 template <int KIND>
-using Q8D128 = Q8Cfg<128, 4, 2, 3, KIND>;
+using Q8D128 = Q8Cfg<128, 8, 1, 3, KIND>;
 template <int KIND>
-using Q8D64 = Q8Cfg<64, 4, 2, 6, KIND>;
+using Q8D64 = Q8Cfg<64, 8, 1, 6, KIND>;
 
 KernelShape q8_shape(int d) {
   const int tile = d == 128 ? Q8D128<1>::kTile : Q8D64<1>::kTile;

@@ -35,7 +35,8 @@ class Workload:
     d_v: int
     n: int                      # cached rows before the first append (all sequences)
     n_max: int                  # cache capacity per sequence
-    dtype: torch.dtype          # q, K, V element type
+    dtype: torch.dtype          # q, K, V element type; torch.int8 / torch.float8_e4m3fn:
+                                # an 8-bit cache of codes with float32 row scales (q bf16)
     kv_std: float = 1.0         # standard deviation of the K/V entries
     q_std: float = 1.0
     ragged: tuple[int, int] | None = None   # lengths ~ U[lo, hi] (inclusive) when set
@@ -73,7 +74,34 @@ WORKLOADS: dict[str, Workload] = {
         "long_llama2_70b", B=2, h_q=64, h_kv=8, d_k=128, d_v=128, n=131072, n_max=131072,
         dtype=torch.bfloat16, kv_std=0.5, num_splits=256,
         description="long context g=8 (Llama-2-70B shape), bf16, B=2, n=131072, 256 splits, K/V ~ N(0, 0.5^2)"),
+    "gqa_llama3_8b_fp8": Workload(
+        "gqa_llama3_8b_fp8", B=16, h_q=32, h_kv=8, d_k=128, d_v=128, n=8192, n_max=8192,
+        dtype=torch.float8_e4m3fn, ragged=(1024, 8192),
+        description="GQA g=4 (Llama-3-8B shape), fp8 e4m3 KV cache with float32 row scales, "
+                    "bf16 q, B=16, lengths ~ U[1024, 8192], n_max=8192"),
+    "gqa_llama3_8b_int8": Workload(
+        "gqa_llama3_8b_int8", B=16, h_q=32, h_kv=8, d_k=128, d_v=128, n=8192, n_max=8192,
+        dtype=torch.int8, ragged=(1024, 8192),
+        description="GQA g=4 (Llama-3-8B shape), int8 KV cache with float32 row scales, "
+                    "bf16 q, B=16, lengths ~ U[1024, 8192], n_max=8192"),
+    "long_llama2_70b_fp8": Workload(
+        "long_llama2_70b_fp8", B=2, h_q=64, h_kv=8, d_k=128, d_v=128, n=131072, n_max=131072,
+        dtype=torch.float8_e4m3fn, kv_std=0.5,
+        description="long context g=8 (Llama-2-70B shape), fp8 e4m3 KV cache with float32 row "
+                    "scales, bf16 q, B=2, n=131072, library's splits"),
 }
+
+Q8_DTYPES = (torch.int8, torch.float8_e4m3fn)
+
+
+def is_q8(w: "Workload") -> bool:
+    """An 8-bit cache: codes plus float32 row scales, q in bf16."""
+    return w.dtype in Q8_DTYPES
+
+
+def _values(w: Workload) -> torch.dtype:
+    """Element type of the generated K/V values: float32 before 8-bit quantization."""
+    return torch.float32 if is_q8(w) else w.dtype
 
 
 def _randn(shape, seed: int, std: float, device="cpu") -> torch.Tensor:
@@ -96,7 +124,8 @@ def seq_lens(w: Workload, seed: int = 0) -> torch.Tensor:
 
 
 def cache(w: Workload, seed: int = 0, poison: bool = False, device="cpu"):
-    """K [B, h_kv, n_max, d_k] and V [B, h_kv, n_max, d_v] in ``w.dtype``.
+    """K [B, h_kv, n_max, d_k] and V [B, h_kv, n_max, d_v] in ``w.dtype`` (float32
+    values, to be quantized, for an 8-bit cache).
 
     Rows at or beyond each sequence's length are filled with NaN when
     ``poison`` is set (a cache's unused rows may hold anything), otherwise
@@ -104,8 +133,8 @@ def cache(w: Workload, seed: int = 0, poison: bool = False, device="cpu"):
     generator runs: a CUDA generator draws other numbers than the CPU one
     from the same seed, so parity inputs are always made on the CPU.
     """
-    K = _randn((w.B, w.h_kv, w.n_max, w.d_k), seed + 0, w.kv_std, device).to(w.dtype)
-    V = _randn((w.B, w.h_kv, w.n_max, w.d_v), seed + 1, w.kv_std, device).to(w.dtype)
+    K = _randn((w.B, w.h_kv, w.n_max, w.d_k), seed + 0, w.kv_std, device).to(_values(w))
+    V = _randn((w.B, w.h_kv, w.n_max, w.d_v), seed + 1, w.kv_std, device).to(_values(w))
     if poison:
         lens = seq_lens(w, seed)
         for b in range(w.B):
@@ -115,14 +144,15 @@ def cache(w: Workload, seed: int = 0, poison: bool = False, device="cpu"):
 
 
 def query(w: Workload, seed: int = 0) -> torch.Tensor:
-    """q [B, h_q, d_k] in ``w.dtype`` (CPU)."""
-    return _randn((w.B, w.h_q, w.d_k), seed + 2, w.q_std).to(w.dtype)
+    """q [B, h_q, d_k] in ``w.dtype`` (bf16 for an 8-bit cache) (CPU)."""
+    return _randn((w.B, w.h_q, w.d_k), seed + 2, w.q_std).to(
+        torch.bfloat16 if is_q8(w) else w.dtype)
 
 
 def new_rows(w: Workload, step: int, seed: int = 0):
     """The key and value rows appended at decode step ``step``: [B, h_kv, d]."""
-    k = _randn((w.B, w.h_kv, w.d_k), seed + 100 + 2 * step, w.kv_std).to(w.dtype)
-    v = _randn((w.B, w.h_kv, w.d_v), seed + 101 + 2 * step, w.kv_std).to(w.dtype)
+    k = _randn((w.B, w.h_kv, w.d_k), seed + 100 + 2 * step, w.kv_std).to(_values(w))
+    v = _randn((w.B, w.h_kv, w.d_v), seed + 101 + 2 * step, w.kv_std).to(_values(w))
     return k, v
 
 

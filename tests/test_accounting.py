@@ -33,3 +33,13 @@ def test_kv_bytes_per_token_examples():
     assert per_token(32, 32) == 512 * 1024      # Llama-2-7B
     assert per_token(80, 8) == 320 * 1024       # Llama-2-70B
     assert per_token(32, 8) == 128 * 1024       # Llama-3-8B
+
+
+def test_q8_bytes_per_row():
+    """An 8-bit row: d codes of one byte plus a float32 scale, for K and for V."""
+    from decode_attention_kv_split_gb300 import accounting
+    one = accounting.decode_bytes_q8([1], 1, 1, 128, 128) - accounting.decode_bytes_q8([0], 1, 1, 128, 128)
+    assert one == 2 * (128 + 4)
+    # bf16 q and fp32 out around them
+    assert accounting.decode_bytes_q8([0], 4, 1, 128, 128) == 4 * 128 * 2 + 4 * 128 * 4
+    assert accounting.append_bytes_q8(2, 3, 64, 64) == 2 * 2 * 3 * (64 + 4 + 64 + 4)

@@ -87,10 +87,42 @@ def test_kv_append_argument_errors(lib):
     assert lib.kv_append(ok, P(20), ok, ok, ok, 1, 1, 64, 64, 8, 0, None, None) == -4
 
 
+def test_q8_argument_errors(lib):
+    """8-bit caches: wrong entry point, missing scales, bad sizes; all before any CUDA call."""
+    P = ctypes.c_void_p
+    ok = P(16)
+
+    def q8(dtype=api.DA_FP8_E4M3, ks=16, vs=16, n_max=8, d=64):
+        return lib.decode_attn_q8_ex(ok, ok, ok, P(ks) if ks else None, P(vs) if vs else None, ok,
+                                     ok, 1, 1, 1, d, d, n_max, 0.125, dtype, 0, None, 0, None, None)
+    assert q8(dtype=api.DA_BF16) == -3                 # not an 8-bit type
+    assert q8(ks=0) == -1                              # scales required
+    assert q8(n_max=6) == -2                           # n_max % 4
+    assert q8(d=96) == -8
+    assert q8(ks=8) == -4                              # scales 16-byte aligned
+    assert _decode_ex(lib, dtype=api.DA_INT8) == -3    # 8-bit cache through the 16/32-bit entry
+    assert _decode_ex(lib, dtype=api.DA_FP8_E4M3 | api.DA_OUT_BF16) == -3
+    assert lib.kv_append(ok, ok, ok, ok, ok, 1, 1, 64, 64, 8, api.DA_INT8, None, None) == -3
+    assert lib.kv_append_q8(ok, ok, None, ok, ok, ok, ok, ok, ok, 1, 1, 64, 64, 8, api.DA_INT8,
+                            None, None) == -1
+    assert lib.kv_append_q8(ok, ok, ok, ok, ok, ok, ok, ok, ok, 1, 1, 64, 64, 8, api.DA_BF16,
+                            None, None) == -3
+    assert lib.kv_quantize(ok, api.DA_FP32, ok, ok, 4, 48, api.DA_INT8, None) == -2   # d % 32
+    assert lib.kv_quantize(ok, api.DA_FP32, ok, ok, 4, 512, api.DA_INT8, None) == -2  # d > 256
+    assert lib.kv_quantize(ok, api.DA_INT8, ok, ok, 4, 64, api.DA_INT8, None) == -3   # x type
+    assert lib.kv_quantize(ok, api.DA_FP32, ok, ok, 4, 64, api.DA_BF16, None) == -3   # code type
+    assert lib.kv_quantize(None, api.DA_FP32, ok, ok, 4, 64, api.DA_INT8, None) == -1
+    assert lib.kv_quantize(ok, api.DA_FP32, ok, ok, 0, 64, api.DA_INT8, None) == 0    # nothing to do
+
+
 def test_header_constants_match_binding():
     text = open(os.path.join(HEADER_DIR, "decode_attn.h")).read()
     defs = dict(re.findall(r"#define\s+(DA_\w+)\s+(0x[0-9a-fA-F]+|\d+)", text))
     assert int(defs["DA_OUT_BF16"], 0) == api.DA_OUT_BF16
+    enum = dict(re.findall(r"(DA_(?:FP32|BF16|INT8|FP8_E4M3))\s*=\s*(\d+)", text))
+    assert {k: int(v) for k, v in enum.items()} == {
+        "DA_FP32": api.DA_FP32, "DA_BF16": api.DA_BF16, "DA_INT8": api.DA_INT8,
+        "DA_FP8_E4M3": api.DA_FP8_E4M3}
     assert int(defs["DA_DEVERR_SEQ_LEN"], 0) == api.DEVERR_SEQ_LEN
     assert int(defs["DA_DEVERR_POS"], 0) == api.DEVERR_POS
     assert int(defs["DA_DEVERR_TIMEOUT"], 0) == api.DEVERR_TIMEOUT

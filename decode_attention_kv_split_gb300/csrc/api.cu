@@ -185,8 +185,11 @@ int check_sizes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype
   if (n_max > (1 << 30)) return DA_ERR_SHAPE;
   if ((long long)B * h_kv * (long long)n_max > 0x7fffffffLL) return DA_ERR_SHAPE;
   if ((long long)B * h_q > 0x7fffffffLL) return DA_ERR_SHAPE;
-  if (d_k != d_v) return DA_ERR_UNSUPPORTED;
-  if (d_k != 64 && d_k != 128) return DA_ERR_UNSUPPORTED;
+  // (d_k, d_v) pairs with kernels: 64/64 and 128/128 for every cache type;
+  // 256/256 and 192/128 for bf16 caches
+  const bool common = (d_k == 64 || d_k == 128) && d_v == d_k;
+  const bool wide = dt.kv == DA_BF16 && ((d_k == 256 && d_v == 256) || (d_k == 192 && d_v == 128));
+  if (!common && !wide) return DA_ERR_UNSUPPORTED;
   if (is_q8(dt.kv) && n_max % 4 != 0) return DA_ERR_SHAPE;  // row-scale tensor map stride
   return DA_OK;
 }
@@ -241,14 +244,15 @@ bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, 
 // the library chooses, the device picks the length from the actual sequence
 // lengths; the host only bounds it from below so that the partial outputs of
 // at most about 4 x SMs work items per launch need workspace.
-int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype_arg, int requested, int sms,
-              Plan* pl) {
+int make_plan(int B, int h_q, int h_kv, int d, int d_v, int n_max, int dtype_arg, int requested,
+              int sms, Plan* pl) {
   const int dtype = dtype_arg & 0xff;
   const int group = h_q / h_kv;
-  pl->tc5 = dtype == DA_BF16 && d == 128 && group > 8;
+  pl->tc5 = dtype == DA_BF16 && d == 128 && d_v == 128 && group > 8;
   pl->ks = pl->tc5 ? da::tc5_shape(group)
            : is_q8(dtype) ? da::q8_shape(d)
-                          : (dtype == DA_BF16 ? da::bf16_shape(d, group) : da::f32_shape(d, group));
+                          : (dtype == DA_BF16 ? da::bf16_shape(d, d_v, group)
+                                              : da::f32_shape(d, group));
   pl->head_chunks = (group + pl->ks.heads_per_cta - 1) / pl->ks.heads_per_cta;
   pl->batch_per_launch = B < da::kMaxBatchPerLaunch ? B : da::kMaxBatchPerLaunch;
   const long long tile = pl->ks.tile_rows;
@@ -274,7 +278,7 @@ int make_plan(int B, int h_q, int h_kv, int d, int n_max, int dtype_arg, int req
   const long long splits = (n_max + pl->chunk_min - 1) / pl->chunk_min;
   if (splits >= (1 << 20)) return DA_ERR_SHAPE;
   pl->max_splits = int(splits);
-  if ((long long)pl->batch_per_launch * h_q * pl->max_splits * (d + 1) > (1LL << 40))
+  if ((long long)pl->batch_per_launch * h_q * pl->max_splits * (d_v + 1) > (1LL << 40))
     return DA_ERR_SHAPE;
   return DA_OK;
 }
@@ -336,9 +340,10 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
   int dev, sms;
   if ((st = current_device(&dev, &sms)) != DA_OK) return st;
   Plan pl;
-  if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
+  if ((st = make_plan(B, h_q, h_kv, d_k, d_v, n_max, dtype, num_splits, sms, &pl)) != DA_OK)
+    return st;
   const size_t out_es = dta.out_bf16 ? 2 : 4;
-  const WorkspaceLayout wl = workspace_layout(pl, h_q, d_k);
+  const WorkspaceLayout wl = workspace_layout(pl, h_q, d_v);
   if (wl.total > 0 && (!workspace || workspace_bytes < wl.total)) return DA_ERR_WORKSPACE;
 
   CUtensorMap tk, tv, tks, tvs;
@@ -392,7 +397,7 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     cudaError_t err =
         pl.tc5 ? da::launch_split_tc5(p, tk, tv, grid, stream)
         : qa   ? da::launch_split_q8(p, tk, tv, tks, tvs, d_k, dtype == DA_INT8 ? 1 : 2, grid, stream)
-        : dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, grid, stream)
+        : dtype == DA_BF16 ? da::launch_split_bf16(p, tk, tv, d_k, d_v, grid, stream)
                            : da::launch_split_f32(p, tk, tv, d_k, grid, stream);
     if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
@@ -437,7 +442,8 @@ int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v, int n
   int dev, sms;
   if ((st = current_device(&dev, &sms)) != DA_OK) return st;
   Plan pl;
-  if ((st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl)) != DA_OK) return st;
+  if ((st = make_plan(B, h_q, h_kv, d_k, d_v, n_max, dtype, num_splits, sms, &pl)) != DA_OK)
+    return st;
   return pl.max_splits;
 }
 
@@ -447,9 +453,9 @@ size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, i
   int dev = 0, sms = 0;
   Plan pl;
   if (st == DA_OK) st = current_device(&dev, &sms);
-  if (st == DA_OK) st = make_plan(B, h_q, h_kv, d_k, n_max, dtype, num_splits, sms, &pl);
+  if (st == DA_OK) st = make_plan(B, h_q, h_kv, d_k, d_v, n_max, dtype, num_splits, sms, &pl);
   if (status) *status = st;
-  return st == DA_OK ? workspace_layout(pl, h_q, d_k).total : 0;
+  return st == DA_OK ? workspace_layout(pl, h_q, d_v).total : 0;
 }
 
 int decode_attn_ex(const void* q, const void* K, const void* V, const int32_t* seq_lens, void* out,

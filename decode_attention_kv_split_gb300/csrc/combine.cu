@@ -134,6 +134,9 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const int
                            const int32_t* seq_lens, int append, void* out, int out_bf16, int B,
                            int h_q, int d,
                            int max_splits, int n_max, cudaStream_t stream) {
+  if (d == 256)
+    return launch_combine_d<256>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
+                                 h_q, max_splits, n_max, stream);
   if (d == 128)
     return launch_combine_d<128>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
                                  h_q, max_splits, n_max, stream);

@@ -229,7 +229,7 @@ struct KernelShape {
   float cta_speed;  // how fast one CTA streams relative to an even share of HBM (measured)
 };
 
-KernelShape bf16_shape(int d, int group);
+KernelShape bf16_shape(int d_k, int d_v, int group);
 KernelShape f32_shape(int d, int group);
 KernelShape tc5_shape(int group);
 KernelShape q8_shape(int d);
@@ -241,7 +241,7 @@ cudaError_t launch_kv_quantize(const void* x, int x_bf16, void* codes, float* sc
 cudaError_t launch_split_tc5(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int grid, cudaStream_t stream);
 cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                              int d, int grid, cudaStream_t stream);
+                              int d_k, int d_v, int grid, cudaStream_t stream);
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
@@ -584,22 +584,20 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
   }
 }
 
-// Fused append: copy the new K and V rows (shared-memory slot, K row then V
-// row, ROW_BYTES each) into row `row` of kv head (b_offset + b, kvh) of the
-// caches.  One warp; an exact copy of the bits.
-template <int ROW_BYTES>
+// Fused append: copy the new K and V rows (shared-memory slot, the K row of
+// KROW bytes then the V row of VROW bytes) into row `it.new_row` of kv head
+// (b_offset + b, kvh) of the caches.  One warp; an exact copy of the bits.
+template <int KROW, int VROW>
 __device__ __forceinline__ void store_new_row(const SplitParams& p, const Item& it,
                                               const uint8_t* slot, int lane) {
   const size_t head = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
-  const size_t off = (head * size_t(p.n_max) + size_t(it.new_row)) * ROW_BYTES;
+  const size_t row = head * size_t(p.n_max) + size_t(it.new_row);
   const uint4* ks = reinterpret_cast<const uint4*>(slot);
-  const uint4* vs = reinterpret_cast<const uint4*>(slot + ROW_BYTES);
-  uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + off);
-  uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(p.v_cache) + off);
-  for (int i = lane; i < ROW_BYTES / 16; i += 32) {
-    kd[i] = ks[i];
-    vd[i] = vs[i];
-  }
+  const uint4* vs = reinterpret_cast<const uint4*>(slot + KROW);
+  uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + row * KROW);
+  uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(p.v_cache) + row * VROW);
+  for (int i = lane; i < KROW / 16; i += 32) kd[i] = ks[i];
+  for (int i = lane; i < VROW / 16; i += 32) vd[i] = vs[i];
 }
 
 // Let a combine kernel launched with programmatic stream serialisation start
@@ -653,15 +651,18 @@ cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int threads, s
 
 // ---------------------------------------------------------------------------
 // Producer: one thread streams every tile of the CTA's items into the ring.
-// NBOX boxes of BOX_COLS columns per tensor per stage, each BOX_BYTES long.
+// A stage holds the K tile (NBOX_K boxes of BOX_COLS columns, BOX_BYTES each)
+// and, V_OFFSET bytes in, the V tile (NBOX_V such boxes).  The item's q rows
+// (QROW bytes each) ride with its first stage, an appended K row (KROW bytes)
+// and V row (VROW bytes) with the stage that holds their position.
 // ---------------------------------------------------------------------------
 // The query rows of an item (its head chunk of one kv group, contiguous in
 // q) ride with the item's first stage into that stage's q slot.
 // With a fused append, the new K and V rows of the unit ride with the stage
 // that holds the unit's last row, into that stage's new-row slot
 // (2 * ROW_BYTES: the K row, then the V row).
-template <int TILE, int STAGES, int STAGE_BYTES, int NBOX, int BOX_COLS, int BOX_BYTES,
-          int HEADS, int ROW_BYTES>
+template <int TILE, int STAGES, int STAGE_BYTES, int NBOX_K, int NBOX_V, int BOX_COLS,
+          int BOX_BYTES, int V_OFFSET, int HEADS, int QROW, int KROW, int VROW>
 __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMap* tmV,
                                         const SplitParams& p, const Schedule& s, uint32_t ring,
                                         uint32_t qslots, uint32_t newslots, uint32_t full0,
@@ -669,7 +670,7 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
   prefetch_tmap(tmK);
   prefetch_tmap(tmV);
   const uint64_t policy = l2_policy_evict_first();
-  constexpr int kTileBytes = STAGE_BYTES / 2;
+  constexpr int kNewSlot = KROW + VROW;
   int stage = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool aborted = false;
@@ -690,31 +691,32 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
       if (HEADS > 0 && t == 0) {
         const int h0 = it.hc * HEADS;
         const int nh = min(HEADS, p.group - h0);
-        extra += uint32_t(nh) * ROW_BYTES;
+        extra += uint32_t(nh) * QROW;
       }
-      if (with_new) extra += 2 * ROW_BYTES;
+      if (with_new) extra += KROW + VROW;
       mbar_arrive_expect_tx(bar, STAGE_BYTES + extra);
       if (HEADS > 0 && t == 0) {
         const int h0 = it.hc * HEADS;
         const int nh = min(HEADS, p.group - h0);
         const char* qsrc = static_cast<const char*>(p.q) +
-                           (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * ROW_BYTES;
-        bulk_load(qslots + stage * (HEADS * ROW_BYTES), qsrc, uint32_t(nh) * ROW_BYTES, bar);
+                           (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * QROW;
+        bulk_load(qslots + stage * (HEADS * QROW), qsrc, uint32_t(nh) * QROW, bar);
       }
       if (with_new) {
-        const size_t src = (size_t(it.b) * p.h_kv + it.kvh) * ROW_BYTES;
-        bulk_load(newslots + stage * (2 * ROW_BYTES), static_cast<const char*>(p.k_new) + src,
-                  ROW_BYTES, bar);
-        bulk_load(newslots + stage * (2 * ROW_BYTES) + ROW_BYTES,
-                  static_cast<const char*>(p.v_new) + src, ROW_BYTES, bar);
+        const size_t src = size_t(it.b) * p.h_kv + it.kvh;
+        bulk_load(newslots + stage * kNewSlot, static_cast<const char*>(p.k_new) + src * KROW,
+                  KROW, bar);
+        bulk_load(newslots + stage * kNewSlot + KROW,
+                  static_cast<const char*>(p.v_new) + src * VROW, VROW, bar);
       }
       const uint32_t kdst = ring + stage * STAGE_BYTES;
       const int y = it.row_begin + t * TILE;
 #pragma unroll
-      for (int h = 0; h < NBOX; ++h) {
+      for (int h = 0; h < NBOX_K; ++h)
         tma_load_3d(kdst + h * BOX_BYTES, tmK, h * BOX_COLS, y, z, bar, policy);
-        tma_load_3d(kdst + kTileBytes + h * BOX_BYTES, tmV, h * BOX_COLS, y, z, bar, policy);
-      }
+#pragma unroll
+      for (int h = 0; h < NBOX_V; ++h)
+        tma_load_3d(kdst + V_OFFSET + h * BOX_BYTES, tmV, h * BOX_COLS, y, z, bar, policy);
       issued |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == STAGES) {

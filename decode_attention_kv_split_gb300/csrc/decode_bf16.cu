@@ -27,15 +27,17 @@
 
 namespace da {
 
-template <int D_, int NB_, int HG_, int KW_, int KBW_, int STAGES_>
+template <int DK_, int DV_, int NB_, int HG_, int KW_, int KBW_, int STAGES_>
 struct Bf16Cfg {
-  static constexpr int D = D_;            // head dim (d_k == d_v)
+  static constexpr int DK = DK_;          // key / query head dim
+  static constexpr int DV = DV_;          // value / output head dim
   static constexpr int NB = NB_;          // 8-head MMA blocks per warp
   static constexpr int HG = HG_;          // head groups (warps sharing rows, different heads)
   static constexpr int KW = KW_;          // key warps per head group
   static constexpr int KBW = KBW_;        // 16-row blocks per key warp per stage
   static constexpr int STAGES = STAGES_;
-  static constexpr int kHalves = D / 64;  // 64-column (128-byte) TMA boxes per row
+  static constexpr int kHalvesK = DK / 64;  // 64-column (128-byte) TMA boxes per K row
+  static constexpr int kHalvesV = DV / 64;
   static constexpr int kTile = 16 * KW * KBW;
   static constexpr int kConsumerWarps = HG * KW;
   static constexpr int kConsumerThreads = 32 * kConsumerWarps;
@@ -43,20 +45,20 @@ struct Bf16Cfg {
   static constexpr int kHPW = 8 * NB;            // heads per warp
   static constexpr int kHeadsPerCta = kHPW * HG;
   static constexpr int kHalfBytes = kTile * 128;
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kSlotStride = D + 4;      // padded row of the epilogue slots
+  static constexpr int kTileBytesK = kTile * DK * 2;  // the K tile; the V tile follows it
+  static constexpr int kStageBytes = kTileBytesK + kTile * DV * 2;
+  static constexpr int kSlotStride = DV + 4;     // padded row of the epilogue slots
   static constexpr int kEpiAccFloats = HG * KW * kHPW * kSlotStride;
   static constexpr int kEpiMLFloats = 2 * HG * KW * kHPW;
   // schedule: first[kMaxBatchPerLaunch + 1], lens[kMaxBatchPerLaunch], red[48]
   // (rounded up to an even count of 4-byte words)
   static constexpr int kSchedWords = da::kSchedWords;  // work list (common.cuh)
-  static constexpr int kQBytes = kHeadsPerCta * D * 2;  // q rows of one item, per stage
-  static constexpr int kNewBytes = 2 * D * 2;              // appended K and V rows, per stage
+  static constexpr int kQBytes = kHeadsPerCta * DK * 2;   // q rows of one item, per stage
+  static constexpr int kNewBytes = (DK + DV) * 2;          // appended K and V rows, per stage
   static constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * (kStageBytes + kQBytes + kNewBytes) +
                                        size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 +
                                        2 * STAGES * 8 + 16;
-  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(DK % 64 == 0 && DV % 64 == 0 && DK <= 256 && DV <= 256, "head dims");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert((kEpiAccFloats + kEpiMLFloats) % 2 == 0, "mbarrier alignment");
 };
@@ -74,9 +76,11 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     split_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-  constexpr int D = Cfg::D, NB = Cfg::NB, KW = Cfg::KW, KBW = Cfg::KBW, STAGES = Cfg::STAGES;
+  constexpr int DK = Cfg::DK, DV = Cfg::DV, NB = Cfg::NB, KW = Cfg::KW, KBW = Cfg::KBW,
+                STAGES = Cfg::STAGES;
   constexpr int kHPW = Cfg::kHPW;
-  constexpr int MB = D / 16;  // 16-wide blocks of d
+  constexpr int MBK = DK / 16;  // 16-wide blocks of d_k (Step I)
+  constexpr int MB = DV / 16;   // 16-wide blocks of d_v (Step III)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -118,8 +122,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   // ------------------------------------------------------------------ producer
   if (warp == Cfg::kConsumerWarps) {
     if (lane == 0)
-      produce<Cfg::kTile, STAGES, Cfg::kStageBytes, Cfg::kHalves, 64, Cfg::kHalfBytes,
-              Cfg::kHeadsPerCta, D * 2>(&tmK, &tmV, p, sched, ring, smem_u32(qslots),
+      produce<Cfg::kTile, STAGES, Cfg::kStageBytes, Cfg::kHalvesK, Cfg::kHalvesV, 64,
+              Cfg::kHalfBytes, Cfg::kTileBytesK, Cfg::kHeadsPerCta, DK * 2, DK * 2, DV * 2>(&tmK, &tmV, p, sched, ring, smem_u32(qslots),
                                         smem_u32(newslots), full0, empty0, abort_flag);
     return;
   }
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // Query heads of this warp: group-local index hl = hc*HeadsPerCta + hg*kHPW + nb*8 + n.
     // Their bf16 rows arrive with the item's first stage (rows past the group are zero).
     const int head_base = it.hc * Cfg::kHeadsPerCta + hg * kHPW;
-    uint32_t qf[NB][MB][2];
+    uint32_t qf[NB][MBK][2];
 
     float m_run[NB][2], l_run[NB][2];
     float acc[MB][NB][4];
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       const uint32_t kbase = ring + stage * Cfg::kStageBytes;
-      const uint32_t vbase = kbase + Cfg::kTileBytes;
+      const uint32_t vbase = kbase + Cfg::kTileBytesK;
       const int tile_row0 = it.row_begin + t * Cfg::kTile;
       const int valid = min(Cfg::kTile, it.row_end - tile_row0);
       const int key0 = kw * KBW * 16;  // first row of this warp inside the stage
@@ -177,15 +181,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           // and (once per kv head) into the caches.
           const uint8_t* slot = newslots + size_t(stage) * Cfg::kNewBytes;
           uint8_t* ktile = smem + size_t(stage) * Cfg::kStageBytes;
-          uint8_t* vtile = ktile + Cfg::kTileBytes;
-          for (int ch = lane; ch < D / 8; ch += 32) {
+          uint8_t* vtile = ktile + Cfg::kTileBytesK;
+          for (int ch = lane; ch < DK / 8; ch += 32) {
             const int col = ch * 8;
             *reinterpret_cast<uint4*>(ktile + swz<Cfg>(new_local, col)) =
                 *reinterpret_cast<const uint4*>(slot + col * 2);
-            *reinterpret_cast<uint4*>(vtile + swz<Cfg>(new_local, col)) =
-                *reinterpret_cast<const uint4*>(slot + D * 2 + col * 2);
           }
-          if (it.hc == 0) store_new_row<D * 2>(p, it, slot, lane);
+          for (int ch = lane; ch < DV / 8; ch += 32) {
+            const int col = ch * 8;
+            *reinterpret_cast<uint4*>(vtile + swz<Cfg>(new_local, col)) =
+                *reinterpret_cast<const uint4*>(slot + DK * 2 + col * 2);
+          }
+          if (it.hc == 0) store_new_row<DK * 2, DV * 2>(p, it, slot, lane);
           fence_proxy_async_smem();
         }
         named_bar_sync(2, Cfg::kConsumerThreads);
@@ -198,9 +205,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const int hloc = hg * kHPW + nb * 8 + r;  // head inside the item
           const bool ok = head_base + nb * 8 + r < p.group;
 #pragma unroll
-          for (int ks = 0; ks < MB; ++ks) {
-            qf[nb][ks][0] = ok ? qs[hloc * (D / 2) + ks * 8 + c] : 0u;
-            qf[nb][ks][1] = ok ? qs[hloc * (D / 2) + ks * 8 + 4 + c] : 0u;
+          for (int ks = 0; ks < MBK; ++ks) {
+            qf[nb][ks][0] = ok ? qs[hloc * (DK / 2) + ks * 8 + c] : 0u;
+            qf[nb][ks][1] = ok ? qs[hloc * (DK / 2) + ks * 8 + 4 + c] : 0u;
           }
         }
       }
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) s[kb][nb][e] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < MB; ++ks) {
+        for (int ks = 0; ks < MBK; ++ks) {
 #pragma unroll
           for (int kb = 0; kb < KBW; ++kb) {
             const int row = key0 + kb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         slot[(h0 + 1) * Cfg::kSlotStride + d0 + 8] = acc[mb][nb][3];
       }
     named_bar_sync(1, Cfg::kConsumerThreads);
-    finish_item<D, Cfg::HG, KW, kHPW, Cfg::kSlotStride>(p, it, epi_acc, epi_m, epi_l, threadIdx.x,
+    finish_item<DV, Cfg::HG, KW, kHPW, Cfg::kSlotStride>(p, it, epi_acc, epi_m, epi_l, threadIdx.x,
                                                         Cfg::kConsumerThreads, abort_flag);
   }
 }
@@ -367,18 +374,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 // ---------------------------------------------------------------------------
 // Variant table and launcher.
 // ---------------------------------------------------------------------------
-using Bf16G8D128 = Bf16Cfg<128, 1, 1, 4, 2, 3>;
-using Bf16G8D64 = Bf16Cfg<64, 1, 1, 4, 2, 6>;
-using Bf16G16D64 = Bf16Cfg<64, 2, 1, 4, 1, 8>;
-using Bf16G32D64 = Bf16Cfg<64, 2, 2, 4, 1, 8>;
+using Bf16G8D128 = Bf16Cfg<128, 128, 1, 1, 4, 2, 3>;
+using Bf16G8D64 = Bf16Cfg<64, 64, 1, 1, 4, 2, 6>;
+using Bf16G16D64 = Bf16Cfg<64, 64, 2, 1, 4, 1, 8>;
+using Bf16G32D64 = Bf16Cfg<64, 64, 2, 2, 4, 1, 8>;
+using Bf16G8D256 = Bf16Cfg<256, 256, 1, 1, 4, 1, 2>;   // 64-row stages of 64 KB
+using Bf16G8D192V128 = Bf16Cfg<192, 128, 1, 1, 4, 1, 3>;
 
 template <class Cfg>
 static KernelShape shape_of() {
   return KernelShape{Cfg::kTile, Cfg::kHeadsPerCta, 64, 1, 1.5f};
 }
 
-KernelShape bf16_shape(int d, int group) {
-  if (d == 128) return shape_of<Bf16G8D128>();  // larger groups use the tcgen05 kernel
+// (d_k, d_v) pairs with a variant; groups above a variant's heads per work
+// item are covered by several head chunks.
+KernelShape bf16_shape(int d_k, int d_v, int group) {
+  if (d_k == 256) return shape_of<Bf16G8D256>();
+  if (d_k == 192) return shape_of<Bf16G8D192V128>();
+  if (d_k == 128) return shape_of<Bf16G8D128>();  // larger groups use the tcgen05 kernel
   if (group <= 8) return shape_of<Bf16G8D64>();
   if (group <= 16) return shape_of<Bf16G16D64>();
   return shape_of<Bf16G32D64>();
@@ -395,8 +408,10 @@ static cudaError_t launch_cfg(const SplitParams& p, const CUtensorMap& tk, const
 }
 
 cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                              int d, int grid, cudaStream_t stream) {
-  if (d == 128) return launch_cfg<Bf16G8D128>(p, tk, tv, grid, stream);
+                              int d_k, int d_v, int grid, cudaStream_t stream) {
+  if (d_k == 256) return launch_cfg<Bf16G8D256>(p, tk, tv, grid, stream);
+  if (d_k == 192) return launch_cfg<Bf16G8D192V128>(p, tk, tv, grid, stream);
+  if (d_k == 128) return launch_cfg<Bf16G8D128>(p, tk, tv, grid, stream);
   if (p.group <= 8) return launch_cfg<Bf16G8D64>(p, tk, tv, grid, stream);
   if (p.group <= 16) return launch_cfg<Bf16G16D64>(p, tk, tv, grid, stream);
   return launch_cfg<Bf16G32D64>(p, tk, tv, grid, stream);

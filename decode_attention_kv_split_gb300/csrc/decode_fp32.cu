@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   // ------------------------------------------------------------------ producer
   if (warp == W) {
     if (lane == 0)
-      produce<Cfg::kTile, STAGES, Cfg::kStageBytes, 1, D, Cfg::kTileBytes, G, D * 4>(
+      produce<Cfg::kTile, STAGES, Cfg::kStageBytes, 1, 1, 0, 0, Cfg::kTileBytes, G, D * 4, D * 4,
+              D * 4>(
           &tmK, &tmV, p, sched, ring, smem_u32(qslots), smem_u32(newslots), full0, empty0,
           abort_flag);
     return;
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             reinterpret_cast<uint4*>(vtile + size_t(new_local) * D * 4)[ch] =
                 reinterpret_cast<const uint4*>(slot + D * 4)[ch];
           }
-          if (it.hc == 0) store_new_row<D * 4>(p, it, slot, lane);
+          if (it.hc == 0) store_new_row<D * 4, D * 4>(p, it, slot, lane);
           fence_proxy_async_smem();
         }
         named_bar_sync(2, Cfg::kConsumerThreads);

@@ -84,7 +84,9 @@ typedef enum {
 #define DA_DEVERR_TIMEOUT 4 /* a pipeline wait exceeded its time limit: outputs invalid */
 
 /*
- * Supported sizes: d_k == d_v, either 64 or 128; any B, h_kv >= 1 and
+ * Supported sizes: d_k == d_v in {64, 128} for every cache type, and for
+ * bf16 caches also d_k == d_v == 256 and d_k = 192 with d_v = 128 (other
+ * pairs return DA_ERR_UNSUPPORTED); any B, h_kv >= 1 and
  * h_q a multiple of h_kv; 1 <= n_max <= 2^30; B * h_kv * n_max rows must fit
  * in 2^31 - 1 for the tensor maps.  Alignment: q, K, V, out, k_new, v_new
  * must be 16-byte aligned.

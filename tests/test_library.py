@@ -70,6 +70,10 @@ def test_argument_errors_return_before_touching_cuda(lib):
     assert _decode_ex(lib, dtype=api.DA_OUT_BF16 | 7) == -3
     assert _decode_ex(lib, d_k=96, d_v=96) == -8           # DA_ERR_UNSUPPORTED
     assert _decode_ex(lib, d_k=64, d_v=128) == -8
+    assert _decode_ex(lib, d_k=256, d_v=256) == -8         # d = 256 only for bf16 caches
+    assert _decode_ex(lib, d_k=192, d_v=128) == -8         # d_k 192 / d_v 128 likewise
+    assert _decode_ex(lib, d_k=192, d_v=64, dtype=api.DA_BF16) == -8
+    assert _decode_ex(lib, d_k=128, d_v=256, dtype=api.DA_BF16) == -8
     assert _decode_ex(lib, scale=float("nan")) == -2
     assert _decode_ex(lib, q=24) == -4                     # DA_ERR_ALIGN
     assert _decode_ex(lib, K=8) == -4

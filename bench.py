@@ -191,7 +191,8 @@ def workload_config(w, n_rot: int, kv_bytes: int):
     cfg = {"workload": w.description, "name": w.name, "B": w.B, "h_q": w.h_q, "h_kv": w.h_kv,
            "d_k": w.d_k, "d_v": w.d_v, "n_start": w.n, "context": f"n+1 .. n+{CYCLE}",
            "n_max_allocated": w.n_max + CYCLE, "kv_dtype": str(w.dtype).replace("torch.", ""),
-           "num_splits": w.num_splits or "auto", "parallelism": "replicas (one per GPU)",
+           "num_splits": {0: "auto", -1: "balanced"}.get(w.num_splits, w.num_splits),
+           "parallelism": "replicas (one per GPU)",
            "tokens_per_step": w.B}
     if w.ragged:
         cfg["lengths"] = f"uniform in [{w.ragged[0]}, {w.ragged[1]}] (seed 3)"

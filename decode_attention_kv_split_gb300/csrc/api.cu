@@ -202,6 +202,8 @@ struct Plan {
   int chunk_min;       // else: the device picks chunk_min * 2^k
   int max_splits;      // partial slots per query head
   int batch_per_launch;
+  bool balanced;       // num_splits = -1: one equal piece of all rows per CTA
+  int units;           // (sequence, kv head, head chunk) units of one launch slice
 };
 
 // The device-side cost model (choose_chunk) evaluated with every sequence at
@@ -257,6 +259,24 @@ int make_plan(int B, int h_q, int h_kv, int d, int d_v, int n_max, int dtype_arg
   pl->batch_per_launch = B < da::kMaxBatchPerLaunch ? B : da::kMaxBatchPerLaunch;
   const long long tile = pl->ks.tile_rows;
   const long long max_tiles = (n_max + tile - 1) / tile;
+  pl->balanced = false;
+  pl->units = int((long long)pl->batch_per_launch * h_kv * pl->head_chunks);
+  if (requested < -1) return DA_ERR_SHAPE;
+  if (requested == -1) {
+    // Balanced pieces when the row stream fits an int and the partials of up
+    // to one per SM per query head stay within 256 MiB; otherwise the
+    // library's usual choice.
+    const long long stream_rows = (long long)pl->units * n_max;
+    const long long part_bytes = (long long)pl->batch_per_launch * h_q * sms * (d_v + 1) * 4;
+    if (stream_rows < (1LL << 31) && part_bytes <= (256LL << 20)) {
+      pl->balanced = true;
+      pl->chunk_fixed = 0;
+      pl->chunk_min = int(tile);
+      pl->max_splits = sms;  // a unit has at most one piece per CTA
+      return DA_OK;
+    }
+    requested = 0;
+  }
   if (requested > 0) {
     long long tiles = (n_max + (long long)requested * tile / 2) / ((long long)requested * tile);
     if (tiles < 1) tiles = 1;
@@ -294,7 +314,8 @@ WorkspaceLayout workspace_layout(const Plan& pl, int h_q, int d) {
   if (pl.max_splits <= 1) return w;
   const size_t heads = size_t(pl.batch_per_launch) * h_q;
   w.header = 0;
-  w.o_part = 256;
+  // header word; in balanced mode the per-unit partial counts follow it
+  w.o_part = pl.balanced ? 256 + (size_t(pl.units) * 4 + 255) / 256 * 256 : 256;
   w.lse_part = w.o_part + heads * pl.max_splits * d * sizeof(float);
   w.total = w.lse_part + heads * pl.max_splits * sizeof(float);
   return w;
@@ -369,6 +390,8 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.o_part = wl.total ? reinterpret_cast<float*>(ws + wl.o_part) : nullptr;
     p.lse_part = wl.total ? reinterpret_cast<float*>(ws + wl.lse_part) : nullptr;
     p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
+    p.balanced = pl.balanced ? 1 : 0;
+    p.unit_nv = pl.balanced ? reinterpret_cast<int*>(ws + 256) : nullptr;
     p.dev_error = dev_error;
     p.append = k_new != nullptr;
     p.k_new = k_new ? static_cast<const char*>(k_new) + size_t(b0) * h_kv * d_k * es : nullptr;
@@ -403,7 +426,8 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     g_launches.fetch_add(1);
     if (wl.total) {
       err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.append, p.out,
-                               p.out_bf16, bn, h_q, d_v, pl.max_splits, n_max, stream);
+                               p.out_bf16, bn, h_q, d_v, pl.max_splits, n_max, p.unit_nv, h_kv,
+                               pl.head_chunks, pl.ks.heads_per_cta, stream);
       if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
       g_launches.fetch_add(1);
     }

@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     lse_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                        const int* __restrict__ chunk_in, const int32_t* __restrict__ seq_lens,
                        int append, void* __restrict__ out, int out_bf16, int h_q, int max_splits,
-                       int n_max) {
+                       int n_max, const int* __restrict__ unit_nv, int h_kv, int head_chunks,
+                       int heads_per_cta) {
   constexpr int EPL = D / 32;
   constexpr int kWarps = kCombineWarps;
   extern __shared__ float csm[];
@@ -58,8 +59,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   n = n < 0 ? 0 : (n > n_max ? n_max : n);
   if (appended) ++n;
   const int chunk = *reinterpret_cast<const volatile int*>(chunk_in);
-  const int nv = n <= 0 ? 1 : (n + chunk - 1) / chunk;
-  if (nv <= 1 || chunk <= 0) return;  // written by the split kernel
+  int nv;
+  if (chunk > 0) {  // chunked list: ceil(n / chunk) splits
+    nv = n <= 0 ? 1 : (n + chunk - 1) / chunk;
+  } else {          // balanced list: the unit's count, written by its first CTA
+    const int group = h_q / h_kv, h = bh - b * h_q;
+    const int kvh = h / group, hc = (h - kvh * group) / heads_per_cta;
+    nv = __ldcg(unit_nv + (b * h_kv + kvh) * head_chunks + hc);
+  }
+  if (nv <= 1) return;  // written by the split kernel
   const float* lse = lse_part + size_t(bh) * max_splits;
   const float* op = o_part + size_t(bh) * max_splits * D + lane * EPL;
 
@@ -120,28 +128,33 @@ template <int D>
 static cudaError_t launch_combine_d(const float* o_part, const float* lse_part,
                                     const int* chunk_in, const int32_t* seq_lens, int append,
                                     void* out, int out_bf16, int B, int h_q, int max_splits, int n_max,
-                                    cudaStream_t stream) {
+                                    const int* unit_nv, int h_kv, int head_chunks,
+                                    int heads_per_cta, cudaStream_t stream) {
   static_assert(kCombineWarps * (D + 2) * 4 <= kCombineSmemBytes, "combine scratch");
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(lse_combine_kernel<D>, kCombineSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   return launch_dependent(lse_combine_kernel<D>, B * h_q, kCombineWarps * 32,
                           size_t(kCombineSmemBytes), stream, o_part, lse_part, chunk_in, seq_lens,
-                          append, out, out_bf16, h_q, max_splits, n_max);
+                          append, out, out_bf16, h_q, max_splits, n_max, unit_nv, h_kv,
+                          head_chunks, heads_per_cta);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
                            const int32_t* seq_lens, int append, void* out, int out_bf16, int B,
-                           int h_q, int d,
-                           int max_splits, int n_max, cudaStream_t stream) {
+                           int h_q, int d, int max_splits, int n_max, const int* unit_nv, int h_kv,
+                           int head_chunks, int heads_per_cta, cudaStream_t stream) {
   if (d == 256)
     return launch_combine_d<256>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
-                                 h_q, max_splits, n_max, stream);
+                                 h_q, max_splits, n_max, unit_nv, h_kv, head_chunks,
+                                 heads_per_cta, stream);
   if (d == 128)
     return launch_combine_d<128>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
-                                 h_q, max_splits, n_max, stream);
+                                 h_q, max_splits, n_max, unit_nv, h_kv, head_chunks,
+                                 heads_per_cta, stream);
   return launch_combine_d<64>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B, h_q,
-                              max_splits, n_max, stream);
+                              max_splits, n_max, unit_nv, h_kv, head_chunks, heads_per_cta,
+                              stream);
 }
 
 }  // namespace da

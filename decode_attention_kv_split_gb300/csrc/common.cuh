@@ -52,6 +52,8 @@ struct SplitParams {
   int n_max;
   int head_chunks;               // query-head chunks per kv head
   int chunk_fixed;               // > 0: rows per split chosen by the caller
+  int balanced;                  // 1: cut all units' rows into one equal piece per CTA
+  int* unit_nv;                  // balanced: [units] partial count of each unit (workspace)
   int chunk_min;                 // else: smallest rows per split the device may choose
   int max_splits;                // partial slots per query head (ceil(n_max / chunk))
   float cta_speed;               // one CTA's streaming rate / its even share (split-length model)
@@ -245,8 +247,9 @@ cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, int append, void* out, int out_bf16, int B, int h_q, int d,
-                           int max_splits, int n_max, cudaStream_t stream);
+                           const int32_t* seq_lens, int append, void* out, int out_bf16, int B,
+                           int h_q, int d, int max_splits, int n_max, const int* unit_nv, int h_kv,
+                           int head_chunks, int heads_per_cta, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void* V,
                              const int32_t* pos, int B, int h_kv, int row_bytes_k,
                              int row_bytes_v, int n_max, const float* ks_new, const float* vs_new,
@@ -276,12 +279,18 @@ constexpr int kSchedWords = kSchedItems + kItemCache * kItemWords;
 
 struct Schedule {
   int* w;           // kSchedWords ints of shared memory:
-                    //   [0, B]      first item of sequence b (first[B] = total)
+                    //   [0, B]      chunked: first item of sequence b (first[B] = total);
+                    //               balanced: stream offset of sequence b's rows per
+                    //               unit, sum of max(n, 1) over earlier sequences
                     //   kSchedLens  rows to decode per sequence; bit 31 set when
                     //               row (len - 1) is appended now
                     //   kSchedItems this CTA's first items, decoded
-  int chunk;
-  int total;
+  int chunk;        // chunked: rows per split
+  int total;        // chunked: items in the list
+  int mine;         // items of this CTA
+  int balanced;     // 1: items are the units one equal piece of the row stream touches
+  int u0;           // balanced: the first unit of this CTA's piece
+  int piece;        // balanced: rows per piece before tile alignment
   __device__ __forceinline__ int first(int b) const { return w[b]; }
   __device__ __forceinline__ int lens(int b) const { return w[kSchedLens + b]; }
 };
@@ -324,11 +333,84 @@ __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedu
   return it;
 }
 
-// Item number i = blockIdx.x + k * gridDim.x of the work list: the k-th item
-// of this CTA, read back from shared memory when build_schedule decoded it.
+// ---------------------------------------------------------------------------
+// Balanced work list.  The rows of every unit, unit after unit (units ordered
+// as in the chunked list; an empty sequence counts one row so that its zero
+// output is still written), form one stream of R rows.  Boundary c of the
+// grid's pieces lies at c * piece, rounded down to a whole tile inside the
+// unit it falls in; CTA c takes the rows between boundaries c and c + 1, an
+// item for every unit they touch.  Every CTA computes the same boundaries.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int bal_len(const Schedule& s, int b) {
+  const int n = len_of(s.lens(b));
+  return n > 0 ? n : 1;
+}
+
+// The unit holding stream position x (0 <= x < R) and the position where it starts.
+__device__ __forceinline__ int bal_unit(const SplitParams& p, const Schedule& s, long long x,
+                                        long long& start) {
+  const long long per_seq = p.h_kv * p.head_chunks;
+  int lo = 0, hi = p.B - 1;  // last b with per_seq * first[b] <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (per_seq * s.first(mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  const long long len = bal_len(s, lo);
+  const long long j = (x - per_seq * s.first(lo)) / len;
+  start = per_seq * s.first(lo) + j * len;
+  return int(lo * per_seq + j);
+}
+
+// Stream position of boundary c (0 .. gridDim.x).
 template <int TILE>
-__device__ __forceinline__ Item cta_item(const SplitParams& p, const Schedule& s, int i, int k) {
-  if (k >= kItemCache) return schedule_item<TILE>(p, s, i);
+__device__ __forceinline__ long long bal_cut(const SplitParams& p, const Schedule& s, int c) {
+  const long long R = (long long)(p.h_kv * p.head_chunks) * s.first(p.B);
+  const long long x = (long long)c * s.piece;
+  if (c <= 0) return 0;
+  if (x >= R) return R;
+  long long start;
+  bal_unit(p, s, x, start);
+  return start + (x - start) / TILE * TILE;
+}
+
+// The item of CTA c on unit u.
+template <int TILE>
+__device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, int c, int u) {
+  const int per_seq = p.h_kv * p.head_chunks;
+  const int b = u / per_seq, j = u - (u / per_seq) * per_seq;
+  const long long len = bal_len(s, b);
+  const long long U = (long long)per_seq * s.first(b) + j * len;
+  const long long lo = bal_cut<TILE>(p, s, c), hi = bal_cut<TILE>(p, s, c + 1);
+  // first CTA whose piece reaches past U; last CTA whose piece starts before U + len
+  int c0 = int(U / s.piece);
+  while (c0 + 1 < int(gridDim.x) && bal_cut<TILE>(p, s, c0 + 1) <= U) ++c0;
+  int c1 = int((U + len - 1) / s.piece);
+  if (c1 > int(gridDim.x) - 1) c1 = int(gridDim.x) - 1;
+  Item it;
+  it.b = b;
+  it.kvh = j / p.head_chunks;
+  it.hc = j - it.kvh * p.head_chunks;
+  it.split = c - c0;
+  it.nv = c1 - c0 + 1;
+  const int n = len_of(s.lens(b));
+  const long long beg = (lo > U ? lo : U) - U;
+  long long end = (hi < U + len ? hi : U + len) - U;
+  if (end > n) end = n;  // an empty sequence's one stream row holds no data
+  it.row_begin = int(beg < end ? beg : end);
+  it.row_end = int(end);
+  const int last = (s.lens(b) & kAppendFlag) ? n - 1 : -1;
+  it.new_row = (last >= it.row_begin && last < it.row_end) ? last : -1;
+  it.tiles = (it.row_end - it.row_begin + TILE - 1) / TILE;
+  return it;
+}
+
+// The k-th item of this CTA (k < s.mine), read back from shared memory when
+// build_schedule decoded it.
+template <int TILE>
+__device__ __forceinline__ Item cta_item(const SplitParams& p, const Schedule& s, int k) {
+  if (k >= kItemCache)
+    return s.balanced ? bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + k)
+                      : schedule_item<TILE>(p, s, int(blockIdx.x) + k * int(gridDim.x));
   const int* w = s.w + kSchedItems + k * kItemWords;
   Item it;
   it.b = w[0];
@@ -458,6 +540,63 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
   Schedule s;
   s.w = sched;
+  s.balanced = 0;
+  s.u0 = 0;
+  s.piece = 0;
+  s.chunk = 0;
+  s.total = 0;
+  s.mine = 0;
+  const int per_seq = p.h_kv * p.head_chunks;
+  if (p.balanced) {
+    __syncthreads();  // lens[] complete
+    if (tid < 32) {   // stream offsets: exclusive scan of max(n, 1) by warp 0
+      int carry = 0;
+      for (int base = 0; base < p.B; base += 32) {
+        const int b = base + tid;
+        const int c = b < p.B ? bal_len(s, b) : 0;
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (tid >= o) x += y;
+        }
+        if (b < p.B) first[b] = carry + x - c;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (tid == 0) first[p.B] = carry;
+    }
+    __syncthreads();
+    s.balanced = 1;
+    const long long R = (long long)per_seq * first[p.B];
+    long long piece = (R + gridDim.x - 1) / gridDim.x;
+    if (piece < TILE) piece = TILE;  // so that no two boundaries round to the same row
+    s.piece = int(piece);
+    const long long lo = bal_cut<TILE>(p, s, int(blockIdx.x));
+    const long long hi = bal_cut<TILE>(p, s, int(blockIdx.x) + 1);
+    if (lo < hi) {
+      long long start;
+      s.u0 = bal_unit(p, s, lo, start);
+      s.mine = bal_unit(p, s, hi - 1, start) - s.u0 + 1;
+    }
+    if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = -1;  // marks balanced
+    for (int t = tid; t < s.mine; t += blockDim.x) {
+      const Item it = bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + t);
+      if (it.split == 0 && p.unit_nv) p.unit_nv[s.u0 + t] = it.nv;  // the unit's first CTA
+      if (t < kItemCache) {
+        int* w = items + t * kItemWords;
+        w[0] = it.b;
+        w[1] = it.kvh;
+        w[2] = it.hc;
+        w[3] = it.split;
+        w[4] = it.nv;
+        w[5] = it.row_begin;
+        w[6] = it.row_end;
+        w[7] = it.new_row;
+      }
+    }
+    __syncthreads();
+    return s;
+  }
   if (p.chunk_fixed > 0) {
     __syncthreads();
     s.chunk = p.chunk_fixed;
@@ -482,7 +621,6 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
     s.chunk = choose_chunk(p, lens, TILE, gridDim.x, all_rows, all_max, red);
   }
   // exclusive scan of items per sequence by warp 0
-  const int per_seq = p.h_kv * p.head_chunks;
   if (tid < 32) {
     int carry = 0;
     for (int base = 0; base < p.B; base += 32) {
@@ -508,6 +646,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = s.chunk;
   // decode this CTA's first items, one per thread
   const int mine = s.total > int(blockIdx.x) ? (s.total - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+  s.mine = mine;
   if (tid < mine && tid < kItemCache) {
     const Item it = schedule_item<TILE>(p, s, int(blockIdx.x) + tid * int(gridDim.x));
     int* w = items + tid * kItemWords;
@@ -674,8 +813,8 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
   int stage = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool aborted = false;
-  for (int i = blockIdx.x, k = 0; i < s.total && !aborted; i += gridDim.x, ++k) {
-    const Item it = cta_item<TILE>(p, s, i, k);
+  for (int k = 0; k < s.mine && !aborted; ++k) {
+    const Item it = cta_item<TILE>(p, s, k);
     const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
     for (int t = 0; t < it.tiles; ++t) {
       if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {

@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
 
-  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
-    const Item it = cta_item<Cfg::kTile>(p, sched, i, k);
+  for (int k = 0; k < sched.mine; ++k) {
+    const Item it = cta_item<Cfg::kTile>(p, sched, k);
 
     // Query heads of this warp: group-local index hl = hc*HeadsPerCta + hg*kHPW + nb*8 + n.
     // Their bf16 rows arrive with the item's first stage (rows past the group are zero).

@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
 
-  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
-    const Item it = cta_item<Cfg::kTile>(p, sched, i, k);
+  for (int k = 0; k < sched.mine; ++k) {
+    const Item it = cta_item<Cfg::kTile>(p, sched, k);
 
     const int head_base = it.hc * G;  // group-local index of this item's first head
     // q (pre-multiplied by scale * log2(e) once loaded, so scores come out in

@@ -152,8 +152,8 @@ __device__ __forceinline__ void produce_q8(const CUtensorMap* tmK, const CUtenso
   int stage = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool aborted = false;
-  for (int i = blockIdx.x, k = 0; i < s.total && !aborted; i += gridDim.x, ++k) {
-    const Item it = cta_item<T>(p, s, i, k);
+  for (int k = 0; k < s.mine && !aborted; ++k) {
+    const Item it = cta_item<T>(p, s, k);
     const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
     for (int t = 0; t < it.tiles; ++t) {
       if (!mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
@@ -299,8 +299,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     return chunk_tensor(u) * Cfg::kF16TileBytes + int(swz_f16<Cfg>(chunk_row(u), chunk_col + c8));
   };
 
-  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
-    const Item it = cta_item<T>(p, sched, i, k);
+  for (int k = 0; k < sched.mine; ++k) {
+    const Item it = cta_item<T>(p, sched, k);
     const int head_base = it.hc * Cfg::kHeadsPerCta;
     const size_t kvhead = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
     uint32_t qf[MB][2];

@@ -191,8 +191,8 @@ __device__ __forceinline__ void produce_ring(const CUtensorMap* map, const void*
   int slot = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool aborted = false;
-  for (int i = blockIdx.x, k = 0; i < s.total && !aborted; i += gridDim.x, ++k) {
-    const Item it = cta_item<T>(p, s, i, k);
+  for (int k = 0; k < s.mine && !aborted; ++k) {
+    const Item it = cta_item<T>(p, s, k);
     const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
     for (int t = 0; t < it.tiles; ++t) {
       if (!mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
@@ -337,8 +337,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t idesc_s = tc5::idesc_bf16(128, NH, 0, 0);
       int kslot = 0;
       uint32_t kphase = 0;
-      for (int i = blockIdx.x, k = 0; i < sched.total && !aborted; i += gridDim.x, ++k) {
-        const Item it = cta_item<T>(p, sched, i, k);
+      for (int k = 0; k < sched.mine && !aborted; ++k) {
+        const Item it = cta_item<T>(p, sched, k);
         if (it.tiles == 0) continue;
         // Q of the item's NH heads, swizzled K-major (rows past the group are
         // zero).  The score MMAs of the previous stage are complete once the
@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t idesc_o = tc5::idesc_bf16(128, 2 * NH, 1, 0);
       int vslot = 0;
       uint32_t vphase = 0;
-      for (int i = blockIdx.x, k = 0; i < sched.total && !aborted; i += gridDim.x, ++k) {
-        const Item it = cta_item<T>(p, sched, i, k);
+      for (int k = 0; k < sched.mine && !aborted; ++k) {
+        const Item it = cta_item<T>(p, sched, k);
         for (int t = 0; t < it.tiles; ++t, ++j) {
           const uint32_t b = j & 1;
           if (!warp_wait(p_full0 + 8 * b, (j >> 1) & 1)) break;
@@ -511,8 +511,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
     tc5::fence_after();
   };
-  for (int i = blockIdx.x, k = 0; i < sched.total; i += gridDim.x, ++k) {
-    const Item it = cta_item<T>(p, sched, i, k);
+  for (int k = 0; k < sched.mine; ++k) {
+    const Item it = cta_item<T>(p, sched, k);
     const int head0 = it.hc * NH;
     const size_t bh0 = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + head0;
     const int nheads = min(NH, p.group - head0);

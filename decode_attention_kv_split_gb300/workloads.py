@@ -41,7 +41,7 @@ class Workload:
     q_std: float = 1.0
     ragged: tuple[int, int] | None = None   # lengths ~ U[lo, hi] (inclusive) when set
     steps: int = 0              # append + decode steps the workload describes
-    num_splits: int = 0         # 0 = let the library choose
+    num_splits: int = 0         # 0 = let the library choose; -1 = balanced pieces
     description: str = ""
 
     @property
@@ -76,14 +76,14 @@ WORKLOADS: dict[str, Workload] = {
         description="long context g=8 (Llama-2-70B shape), bf16, B=2, n=131072, 256 splits, K/V ~ N(0, 0.5^2)"),
     "gqa_llama3_8b_fp8": Workload(
         "gqa_llama3_8b_fp8", B=16, h_q=32, h_kv=8, d_k=128, d_v=128, n=8192, n_max=8192,
-        dtype=torch.float8_e4m3fn, ragged=(1024, 8192),
+        dtype=torch.float8_e4m3fn, ragged=(1024, 8192), num_splits=-1,
         description="GQA g=4 (Llama-3-8B shape), fp8 e4m3 KV cache with float32 row scales, "
-                    "bf16 q, B=16, lengths ~ U[1024, 8192], n_max=8192"),
+                    "bf16 q, B=16, lengths ~ U[1024, 8192], n_max=8192, balanced pieces"),
     "gqa_llama3_8b_int8": Workload(
         "gqa_llama3_8b_int8", B=16, h_q=32, h_kv=8, d_k=128, d_v=128, n=8192, n_max=8192,
-        dtype=torch.int8, ragged=(1024, 8192),
+        dtype=torch.int8, ragged=(1024, 8192), num_splits=-1,
         description="GQA g=4 (Llama-3-8B shape), int8 KV cache with float32 row scales, "
-                    "bf16 q, B=16, lengths ~ U[1024, 8192], n_max=8192"),
+                    "bf16 q, B=16, lengths ~ U[1024, 8192], n_max=8192, balanced pieces"),
     "long_llama2_70b_fp8": Workload(
         "long_llama2_70b_fp8", B=2, h_q=64, h_kv=8, d_k=128, d_v=128, n=131072, n_max=131072,
         dtype=torch.float8_e4m3fn, kv_std=0.5,

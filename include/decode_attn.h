@@ -120,7 +120,13 @@ DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int
  *   seq_lens     : device int32 [B]; 0 <= seq_lens[b] <= n_max.  Values out
  *                  of range are clamped and flagged in *dev_error.
  *   scale        : multiplies q.K (typically 1/sqrt(d_k)).
- *   num_splits   : splits per (b, kv head); 0 = library's choice.
+ *   num_splits   : splits per (b, kv head); 0 = library's choice; -1 =
+ *                  balanced: the rows of all (sequence, kv head) units, unit
+ *                  after unit, are cut into one equal piece per SM (at tile
+ *                  boundaries), for batches whose lengths differ widely (the
+ *                  workspace then holds up to one partial per SM per query
+ *                  head; when that exceeds 256 MiB, or the rows of a launch
+ *                  slice exceed 2^31, the library's choice applies).
  *   workspace    : device memory of at least
  *                  decode_attn_workspace_bytes(...) bytes, 16-byte aligned;
  *                  may be NULL when that is 0.  Its contents need no

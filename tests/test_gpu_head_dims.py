@@ -55,7 +55,7 @@ def _check(got, want):
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"hq{c[1]}_hkv{c[2]}_dk{c[3]}_dv{c[4]}_n{c[5]}" for c in CASES])
-@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("splits", [0, 1, 3, -1])
 def test_decode_wide_heads(o, case, splits):
     B, h_q, h_kv, dk, dv, n_max, lens = case
     w, q, K, V, lens_t = _case(B, h_q, h_kv, dk, dv, n_max, lens, seed=dk + h_q)

@@ -85,7 +85,7 @@ SWEEP = [
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 @pytest.mark.parametrize("case", SWEEP, ids=[f"B{c[0]}_hq{c[1]}_hkv{c[2]}_d{c[3]}_n{c[4]}" for c in SWEEP])
-@pytest.mark.parametrize("splits", [0, 1, 3, 1000])
+@pytest.mark.parametrize("splits", [0, 1, 3, 1000, -1])
 def test_decode_matches_oracle(o, dtype, case, splits):
     B, h_q, h_kv, d, n_max, lens = case
     q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=len(lens) + d)
@@ -297,9 +297,33 @@ def test_batch_larger_than_one_launch_slice(o, dtype):
     rng = np.random.default_rng(4)
     lens = [int(x) for x in rng.integers(0, 70, B)]
     q, K, V, lens_t, scale = make_case(B, 4, 2, 64, 70, lens, dtype, seed=5)
-    for splits in (0, 1, 3):
+    for splits in (0, 1, 3, -1):
         out = gpu_decode(q, K, V, lens_t, num_splits=splits)
         check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
+# ----------------------------------------------------------------- balanced pieces (num_splits = -1)
+BALANCED = [
+    # B, h_q, h_kv, d, n_max, dtype; lengths drawn in [0, n_max] with zeros and full rows forced
+    (16, 32, 8, 128, 3000, torch.bfloat16),   # GQA group 4 (mma.sync kernel)
+    (6, 32, 1, 128, 5000, torch.bfloat16),    # MQA (tcgen05 kernel)
+    (12, 8, 8, 64, 2000, torch.float32),      # MHA (fp32 kernel)
+    (40, 16, 2, 64, 700, torch.bfloat16),     # many short units, group 8, d = 64
+    (3, 64, 1, 64, 900, torch.bfloat16),      # group 64: two head chunks
+]
+
+
+@pytest.mark.parametrize("case", BALANCED, ids=[f"B{c[0]}_hq{c[1]}_hkv{c[2]}_d{c[3]}_{str(c[5])[6:]}" for c in BALANCED])
+def test_balanced_pieces_ragged(o, case):
+    """One equal piece of the concatenated rows per CTA: units cut at arbitrary
+    tile boundaries, several units per CTA, empty and full sequences."""
+    B, h_q, h_kv, d, n_max, dtype = case
+    rng = np.random.default_rng(B + d)
+    lens = [int(x) for x in rng.integers(0, n_max + 1, B)]
+    lens[0], lens[-1] = 0, n_max
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=B)
+    out = gpu_decode(q, K, V, lens_t, num_splits=-1)
+    check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
 
 
 # ----------------------------------------------------------------- fused append + decode
@@ -318,7 +342,7 @@ APPEND_CASES = [
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 @pytest.mark.parametrize("case", APPEND_CASES, ids=[f"case{i}" for i in range(len(APPEND_CASES))])
-@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("splits", [0, 1, 3, -1])
 def test_fused_append_decode(o, dtype, case, splits):
     B, h_q, h_kv, d, n_max, lens = case
     q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=B + h_q)

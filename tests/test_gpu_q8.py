@@ -115,7 +115,7 @@ CASES = [
 
 @pytest.mark.parametrize("kind", list(KINDS))
 @pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}_hq{c[1]}_hkv{c[2]}_d{c[3]}_n{c[4]}" for c in CASES])
-@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("splits", [0, 1, 3, -1])
 def test_q8_decode_matches_oracle(o, kind, case, splits):
     B, h_q, h_kv, d, n_max, lens = case
     k = KINDS[kind][0]
@@ -192,7 +192,7 @@ APPEND_CASES = [
 
 @pytest.mark.parametrize("kind", list(KINDS))
 @pytest.mark.parametrize("case", APPEND_CASES, ids=[f"case{i}" for i in range(len(APPEND_CASES))])
-@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("splits", [0, 1, 3, -1])
 def test_q8_fused_append_decode(o, kind, case, splits):
     k, tdt = KINDS[kind]
     B, h_q, h_kv, d, n_max, lens = case

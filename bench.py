@@ -18,6 +18,7 @@ over ranks and ``value`` counts all ranks' tokens.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -187,18 +188,48 @@ def replica_rate(local_ms: float, world: int, units_per_rank: int, steps: int):
     return ms_per_step, world * units_per_rank / (ms_per_step / 1e3)
 
 
-def workload_config(w, n_rot: int, kv_bytes: int):
-    cfg = {"workload": w.description, "name": w.name, "B": w.B, "h_q": w.h_q, "h_kv": w.h_kv,
-           "d_k": w.d_k, "d_v": w.d_v, "n_start": w.n, "context": f"n+1 .. n+{CYCLE}",
-           "n_max_allocated": w.n_max + CYCLE, "kv_dtype": str(w.dtype).replace("torch.", ""),
-           "num_splits": {0: "auto", -1: "balanced"}.get(w.num_splits, w.num_splits),
+def padded(w):
+    """The workload as the bench allocates it: room for the CYCLE appended rows."""
+    return W.custom(name=w.name, B=w.B, h_q=w.h_q, h_kv=w.h_kv, d_k=w.d_k, d_v=w.d_v, n=w.n,
+                    n_max=w.n_max + CYCLE, dtype=w.dtype, kv_std=w.kv_std, ragged=w.ragged,
+                    num_splits=w.num_splits, description=w.description)
+
+
+def decode_bytes_of(w, lens) -> int:
+    """Algorithmic bytes of one decode over the given lengths."""
+    if W.is_q8(w):
+        return accounting.decode_bytes_q8(lens, w.h_q, w.h_kv, w.d_k, w.d_v)
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    return accounting.decode_bytes(lens, w.h_q, w.h_kv, w.d_k, w.d_v, es)
+
+
+def rotation(w):
+    """(K/V copies the bench rotates through, bytes one step touches): enough copies
+    that the cache bytes read between two uses of one copy exceed 4x the L2."""
+    kv_touch = decode_bytes_of(w, (W.seq_lens(w) + CYCLE).tolist())
+    return int(min(64, max(1, math.ceil(4 * L2_BYTES / kv_touch)))), kv_touch
+
+
+def workload_config(wb):
+    """The ``config`` object of a bench line: depends on the workload alone, so that
+    both arms print the same one."""
+    n_rot, kv_bytes = rotation(wb)
+    cfg = {"workload": wb.description, "name": wb.name, "B": wb.B, "h_q": wb.h_q,
+           "h_kv": wb.h_kv, "d_k": wb.d_k, "d_v": wb.d_v, "n_start": wb.n,
+           "context": f"n+1 .. n+{CYCLE}", "n_max_allocated": wb.n_max,
+           "kv_dtype": str(wb.dtype).replace("torch.", ""),
+           "num_splits": {0: "auto", -1: "balanced"}.get(wb.num_splits, wb.num_splits),
            "parallelism": "replicas (one per GPU)",
-           "tokens_per_step": w.B}
-    if w.ragged:
-        cfg["lengths"] = f"uniform in [{w.ragged[0]}, {w.ragged[1]}] (seed 3)"
-    if n_rot * kv_bytes >= 4 * L2_BYTES:
-        cfg["l2"] = (f"{n_rot} rotating K/V copies of {kv_bytes / 1e6:.0f} MB each "
-                     f"(>= 4x the {L2_BYTES >> 20} MiB L2 between reuses)")
+           "tokens_per_step": wb.B}
+    if wb.ragged:
+        cfg["lengths"] = f"uniform in [{wb.ragged[0]}, {wb.ragged[1]}] (seed 3)"
+    if n_rot * kv_bytes >= 4 * L2_BYTES and n_rot == 1:
+        cfg["l2"] = (f"inputs larger than L2: one K/V cache of {kv_bytes / 1e6:.0f} MB per step "
+                     f"(>= 4x the {L2_BYTES >> 20} MiB L2)")
+    elif n_rot * kv_bytes >= 4 * L2_BYTES:
+        cfg["l2"] = (f"inputs larger than L2: {n_rot} rotating K/V copies of "
+                     f"{kv_bytes / 1e6:.0f} MB each (>= 4x the {L2_BYTES >> 20} MiB L2 "
+                     "between reuses)")
     else:
         cfg["l2"] = (f"L2-resident: {n_rot} K/V copies of {kv_bytes / 1e6:.2f} MB; "
                      "latency only, GB/s not meaningful")
@@ -206,58 +237,94 @@ def workload_config(w, n_rot: int, kv_bytes: int):
 
 
 # --------------------------------------------------------------------------- oracle timing
-def oracle_step_sample(w, budget_s: float, threads: int):
-    """Time the oracle's decode on a bounded sample of the workload's (b, h)
-    heads at context n+1.  Returns (tokens/s equivalent, sample text, cores)."""
-    import numpy as np
-    import oracle
+class OracleStep:
+    """The CPU oracle run on the bench's own workload: one step appends the new K/V
+    row of every (sequence, kv head) and decodes every query head over the grown
+    cache, exactly the step the GPU arm times (oracle ``kv_append`` then
+    ``decode``, fp64 arithmetic on the same rounded inputs).  An 8-bit cache is
+    timed on its float32 values before quantization: the oracle's decode does
+    the same work on any values."""
 
-    o = oracle.get()
-    cores = min(threads, o.max_threads())
-    lens = W.seq_lens(w)
-    q = W.query(w).float().numpy()
-    # one kv head's rows are shared by its group; sample whole groups of heads
-    n1 = int(lens[0]) + 1
-    g = np.random.default_rng(0)
-    Kh = g.standard_normal((n1, w.d_k)).astype(np.float32)
-    Vh = g.standard_normal((n1, w.d_v)).astype(np.float32)
+    def __init__(self, w):
+        import numpy as np
+        import oracle
+
+        self.o = oracle.get()
+        self.wb = wb = padded(w)
+        self.lens0 = W.seq_lens(wb).numpy().astype(np.int32)
+        vals = torch.float32 if W.is_q8(wb) else wb.dtype
+        K, V = W.cache(dataclasses.replace(wb, dtype=vals))
+        self.K = np.ascontiguousarray(K.float().numpy())
+        self.V = np.ascontiguousarray(V.float().numpy())
+        del K, V
+        self.q = np.ascontiguousarray(W.query(wb).float().numpy())
+        rows = [W.new_rows(wb, t) for t in range(CYCLE)]
+        self.rows = [(np.ascontiguousarray(k.float().numpy()),
+                      np.ascontiguousarray(v.float().numpy())) for k, v in rows]
+        self.cores = self.o.max_threads()
+
+    def step(self, i: int, threads: int, seqs=None):
+        """Append at position n + (i mod CYCLE), decode over one row more.  ``seqs``
+        limits the step to the first ``seqs`` sequences (a bounded sample)."""
+        c = i % CYCLE
+        kn, vn = self.rows[c]
+        pos = self.lens0 + c
+        self.o.kv_append(kn, vn, self.K, self.V, pos)
+        b = self.wb.B if seqs is None else seqs
+        self.o.decode(self.q[:b], self.K[:b], self.V[:b], (pos + 1)[:b], self.wb.scale,
+                      threads=threads)
+
+    def rows_of(self, seqs=None) -> float:
+        b = self.wb.B if seqs is None else seqs
+        return float(self.lens0[:b].sum()) + b * (CYCLE + 1) / 2
+
+
+def oracle_baseline(w, seconds: float):
+    """cpu_baseline of a bench line: the oracle timed on the host cores on the
+    workload itself (whole steps, all cores), plus a one-core figure from a
+    one-sequence sample of a step, scaled to the whole step by its rows."""
+    st = OracleStep(w)
+    cores = st.cores
+    st.step(0, cores)  # first touch of the arrays
     t0 = time.perf_counter()
-    heads = 0
-    while True:
-        o.decode_head(q[0, heads % w.h_q], Kh, Vh, w.scale)
-        heads += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
+    steps = 0
+    while steps < 1 or time.perf_counter() - t0 < seconds / 2:
+        st.step(1 + steps, cores)
+        steps += 1
     el = time.perf_counter() - t0
-    # every token needs B*h_q heads at this context length (ragged: mean length)
-    mean_len = float(lens.double().mean()) + 1
-    heads_per_token = w.h_q * (mean_len / n1)
-    tok_s = heads / heads_per_token / el
-    return tok_s, (f"oracle decode_head (fp64, 1 thread) on {heads} single heads at n={n1} "
-                   f"for {el:.1f} s, scaled to B*h_q heads per token at mean context "
-                   f"{mean_len:.0f}"), 1
+    tok_s = st.wb.B * steps / el
+    t1 = time.perf_counter()
+    st.step(0, 1, seqs=1)
+    el1 = time.perf_counter() - t1
+    tok_s_1 = st.wb.B / (el1 * st.rows_of() / st.rows_of(1))
+    sample = (f"oracle kv_append + decode (fp64) on the workload itself: {steps} whole step(s) "
+              f"on {cores} threads in {el:.2f} s; one-core figure from sequence 0 of a step "
+              f"({el1:.2f} s) scaled to the step's rows")
+    return {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "value_1core": tok_s_1}
 
 
 def run_reference(args, w, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on the host cores (rank 0
+    only), over the same workload, metric and config as the GPU arm."""
     if rank != 0:
         return
-    budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        oracle_step_sample(w, budget / 4, 1)
+    st = OracleStep(w)
+    cores = st.cores
+    for i in range(args.warmup):
+        st.step(i, cores)
     t0 = time.perf_counter()
-    vals = []
-    sample = ""
-    for _ in range(args.steps):
-        v, sample, cores = oracle_step_sample(w, budget, 1)
-        vals.append(v)
+    for i in range(args.steps):
+        st.step(args.warmup + i, cores)
     el = time.perf_counter() - t0
-    value = sum(vals) / len(vals)
+    value = st.wb.B * args.steps / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, 1, 0),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "data": "synthetic", "config": workload_config(st.wb),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"oracle kv_append + decode (fp64), {args.steps} whole "
+                                       f"steps of the workload on {cores} threads"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -273,21 +340,18 @@ class Harness:
         self.api = api
         dev = torch.device("cuda", torch.cuda.current_device())
         torch.manual_seed(rank)
-        n_max = w.n_max + CYCLE
-        wb = W.custom(name=w.name, B=w.B, h_q=w.h_q, h_kv=w.h_kv, d_k=w.d_k, d_v=w.d_v, n=w.n,
-                      n_max=n_max, dtype=w.dtype, kv_std=w.kv_std, ragged=w.ragged,
-                      num_splits=w.num_splits, description=w.description)
+        wb = padded(w)
+        n_max = wb.n_max
         seed = 1000 * rank
         lens0 = W.seq_lens(wb, seed)
         self.q8 = W.is_q8(w)
         es = 1 if self.q8 else (2 if w.dtype == torch.bfloat16 else 4)
         row_bytes = (w.d_k + 4) if self.q8 else w.d_k * es  # an 8-bit row carries its scale
         self.w, self.es = w, es
-        kv_touch = self._decode_bytes((lens0 + CYCLE).tolist())
-        n_rot = max(1, math.ceil(4 * L2_BYTES / kv_touch))
+        n_rot, kv_touch = rotation(wb)
         cache_bytes = 2 * wb.B * wb.h_kv * n_max * row_bytes
         free = torch.cuda.mem_get_info(dev)[0]
-        n_rot = int(max(1, min(n_rot, 64, (0.6 * free) // cache_bytes)))
+        n_rot = int(max(1, min(n_rot, (0.6 * free) // cache_bytes)))
 
         K0, V0 = W.cache(wb, seed, device=dev if gpu_cache else "cpu")
         K0, V0 = K0.to(dev), V0.to(dev)
@@ -378,14 +442,15 @@ class Harness:
 
     def time_steps(self, K: int, world: int = 1, graph=None) -> float:
         """Device time in ms of K consecutive steps, from one CUDA event pair on the
-        stream: a replay of `graph` (K steps recorded by capture()), or K eager calls."""
+        stream, bracketed by a barrier and a device synchronize on both sides: a
+        replay of `graph` (K steps recorded by capture()), or K eager calls."""
         ev_start = torch.cuda.Event(enable_timing=True)
         ev_end = torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         # Keep the GPU busy (outside the timed region) while the host queues the
-        # first steps, so that host launch latency does not leak into the timing.
-        torch.cuda._sleep(int(5e7))
+        # steps, so that host launch latency does not leak into the timing.
+        torch.cuda._sleep(int(2e6 if graph is not None else 2e6 + 8e4 * K))
         ev_start.record(self.stream)
         if graph is not None:
             graph.replay()
@@ -396,6 +461,15 @@ class Harness:
         torch.cuda.synchronize()
         barrier(world)
         return ev_start.elapsed_time(ev_end)
+
+    def time_windows(self, K: int, world: int, graph=None, min_s: float = 0.8):
+        """Repeated K-step windows (each timed as time_steps does) until about
+        `min_s` seconds of device time have passed, at least 5 and at most 400
+        windows, the same count on every rank.  Returns the window times in ms."""
+        first = self.time_steps(K, world, graph)
+        reps = int(min(400, max(5, math.ceil(min_s * 1e3 / max(first, 1e-3)))))
+        reps = int(max_over_ranks(reps, world))
+        return [self.time_steps(K, world, graph) for _ in range(reps)]
 
 
 def run_ours(args, w, world, rank, local):
@@ -416,17 +490,21 @@ def run_ours(args, w, world, rank, local):
     K = args.steps
     graph = None
     if not args.eager:
-        graph, launches = h.capture(K)
+        graph, launches_per_window = h.capture(K)
         h.time_steps(K, world, graph)  # first replay: uploads the graph
     launches0 = api.launch_count()
     if sampler:
         sampler.mark(True)
-    local_ms = h.time_steps(K, world, graph)
+    windows = h.time_windows(K, world, graph)
     if sampler:
         sampler.mark(False)
     if args.eager:
         launches = api.launch_count() - launches0
+        launches_per_window = launches // (len(windows) + 1)
+    else:
+        launches = launches_per_window * len(windows)
     del graph
+    local_ms = sorted(windows)[len(windows) // 2]  # median window
     ms_per_step, tokens_per_s = replica_rate(local_ms, world, w.B, K)
     clocks = sampler.stop() if sampler else None
 
@@ -448,7 +526,7 @@ def run_ours(args, w, world, rank, local):
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
-    e2e_steps = max(1, min(K, 2000))
+    e2e_steps = min(2000, max(K, 200))
     for i in range(min(args.warmup, 8)):
         e2e_step(i)
     barrier(world)
@@ -467,17 +545,17 @@ def run_ours(args, w, world, rank, local):
     achieved = step_bytes / (ms_per_step / 1e3) / 1e9
     traffic = recorded_traffic(w.name)
     bytes_str = f"{step_bytes / 1e6:.1f} MB per step"
-    if w.B * w.h_kv * w.n * (w.d_k + w.d_v) * h.es < L2_BYTES:
+    if h.n_rot * h.kv_touch < 4 * L2_BYTES:
         bytes_str += " (L2-resident)"
 
-    cpu_v, cpu_sample, cpu_cores = oracle_step_sample(wb, args.cpu_seconds, 1)
+    cpu = oracle_baseline(w, args.cpu_seconds)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("f16 (8-bit codes, fp32 scales)" if h.q8
                   else "f32" if w.dtype == torch.float32 else "bf16"),
-        "data": "synthetic", "config": workload_config(wb, n_rot, kv_touch),
+        "data": "synthetic", "config": workload_config(wb),
         "hbm_gbs": achieved,
         "hbm_frac_of_8tbs": achieved / 8000.0,
         "step": "decode_attn_append (fused append + decode)" if fused
@@ -489,18 +567,21 @@ def run_ours(args, w, world, rank, local):
                      + (" (+ PDL LSE combine)" if splits > 1 else ""),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "timing": "CUDA events around the K timed steps on the launching stream; "
-                               "one kernel per step (two when splits are merged)",
+                     "timing": "CUDA events on the launching stream around each window of K "
+                               "steps; median window",
                      "traffic": traffic, "algorithmic_bytes": step_bytes, "per": bytes_str},
-        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
-                         "sample": cpu_sample},
+        "cpu_baseline": cpu,
         "e2e": {"value": e2e_rate, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "sync": "host waits for each step's result"},
         "gpu_launches": launches,
+        "gpu_launches_per_step": launches_per_window / K,
         "launch": ("eager: one C-ABI call per step" if args.eager else
                    "the K steps recorded once through the C-ABI into a CUDA graph, "
-                   "replayed once inside the timed region"),
+                   "replayed once per timed window"),
+        "windows": {"count": len(windows), "steps_each": K,
+                    "ms_min": min(windows), "ms_median": local_ms, "ms_max": max(windows),
+                    "value_from": "median window"},
         "clocks": clocks,
     }
     print(json.dumps(line))
@@ -560,7 +641,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mha_fp32", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="long_llama2_70b", choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--separate-append", action="store_true",
                     help="run kv_append and decode_attn as two launches instead of the fused call")

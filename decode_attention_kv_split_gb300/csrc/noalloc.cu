@@ -13,9 +13,10 @@
 // The buffer is a file-scope __device__ array, so every GPU that loads this
 // library holds it (kNoAllocScratchBytes) until the process exits.  In host
 // code the array's name is only a host-side stand-in for the symbol, never a
-// usable device address: the address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made on
-// that device, and cached.
+// usable device address: the address is looked up with cudaGetSymbolAddress,
+// with the device current, on the first call made on that device, and cached
+// together with the id of the context it belongs to; a call from a newer
+// context of the device (after cudaDeviceReset) looks it up again.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,23 +30,69 @@ constexpr size_t kNoAllocScratchBytes = size_t(DA_NOALLOC_SCRATCH_BYTES);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxNoAllocDevices = 64;
-void* g_scratch_addr[kMaxNoAllocDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // the context the address belongs to (0: none yet)
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxNoAllocDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of g_noalloc_scratch on the current device.
+// Driver entry points (no libcuda link): the current context and its
+// process-unique id, so that an address looked up in a context that has since
+// been destroyed (cudaDeviceReset) is never reused.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::once_flag g_ctx_fns_once;
+
+int current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_fns_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return DA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return DA_ERR_CUDA;
+  if (g_ctx_get_id(ctx, id) != CUDA_SUCCESS) return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+// Device address of g_noalloc_scratch in the current device's context.
 int scratch_address(void** addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return DA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxNoAllocDevices) return DA_ERR_DEVICE;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return DA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  unsigned long long ctx_id = 0;
+  int st = current_context_id(&ctx_id);
+  void* fresh = nullptr;
+  if (st != DA_OK) {
+    // No context bound to this thread yet: the symbol lookup binds the
+    // device's primary context (the one the launch will use); read its id then.
+    e = cudaGetSymbolAddress(&fresh, g_noalloc_scratch);
+    if (e != cudaSuccess || fresh == nullptr) return DA_ERR_CUDA;
+    if ((st = current_context_id(&ctx_id)) != DA_OK) return st;
   }
-  *addr = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  ScratchEntry& ent = g_scratch[dev];
+  if (ent.ctx_id != ctx_id || !ent.addr) {
+    void* p = fresh;
+    if (!p) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr) return DA_ERR_CUDA;
+    }
+    ent.addr = p;
+    ent.ctx_id = ctx_id;
+  }
+  *addr = ent.addr;
   return DA_OK;
 }
 

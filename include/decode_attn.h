@@ -195,10 +195,14 @@ DA_API int decode_attn(const void* q, const void* K, const void* V, const int32_
  *
  * Returns DA_ERR_WORKSPACE when the request needs more scratch than
  * DA_NOALLOC_SCRATCH_BYTES (see decode_attn_workspace_bytes; fewer splits
- * need less).  Calls no cudaMalloc, cudaFree or other allocating routine.
- * The first call on a device looks up the buffer's device address with that
- * device current and caches it; make that first call before any stream
- * capture.  All calls share the one buffer, which keeps the last call's
+ * need less).  Balanced pieces (num_splits = -1) keep up to one partial per
+ * SM per query head, which exceeds the buffer for all but small batches
+ * (B = 16, h_q = 32, d_v = 128 already needs ~39 MB): such requests are
+ * rejected, not served with another split choice.  Calls no cudaMalloc,
+ * cudaFree or other allocating routine.  The first call on a device looks up
+ * the buffer's device address with that device current and caches it with
+ * the id of the device's current context (a call after cudaDeviceReset looks
+ * it up again); make that first call before any stream capture.  All calls share the one buffer, which keeps the last call's
  * contents (nothing in it needs to start at zero): calls whose kernels may
  * overlap on the GPU (different streams, or several host threads) race on it
  * and must be serialised by the caller.

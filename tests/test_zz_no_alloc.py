@@ -57,6 +57,7 @@ CASES = [
     (1, 32, 1, 128, 8192, [8192], torch.bfloat16, 32),
     (3, 8, 8, 64, 777, [777, 1, 400], torch.float32, 5),
     (2, 4, 4, 128, 300, [300, 0], torch.float32, 1),
+    (2, 8, 2, 128, 2000, [2000, 333], torch.bfloat16, -1),   # balanced: per-unit table too
 ]
 
 
@@ -87,8 +88,14 @@ def test_noalloc_rejects_requests_beyond_its_scratch(lib):
     B, h_q, h_kv, d, n_max = 64, 64, 8, 128, 131072
     need = api.workspace_bytes(B, h_q, h_kv, d, d, n_max, torch.bfloat16, 1024)
     assert need > SCRATCH_LIMIT
-    P = ctypes.c_void_p
-    fake = P(256)   # never dereferenced: the size check fails first
-    st = lib.decode_attn_noalloc(fake, fake, fake, fake, fake, B, h_q, h_kv, d, d, n_max, 0.1, 1,
-                                 1024, None, None)
+    # Real (small) device buffers: the call must refuse on the sizes alone, but
+    # nothing it is handed is a bogus address should that order ever change.
+    dev = torch.device("cuda")
+    bufs = [torch.zeros(64, dtype=torch.int32, device=dev) for _ in range(5)]
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.decode_attn_noalloc(*[P(t) for t in bufs], B, h_q, h_kv, d, d, n_max, 0.1, 1, 1024,
+                                 None, stream)
     assert st == -5   # DA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert all(bool((t == 0).all()) for t in bufs)

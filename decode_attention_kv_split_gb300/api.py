@@ -58,6 +58,9 @@ SIGNATURES = {
                                    _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
     "kv_append_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "kv_quantize": (_I, [_P, _I, _P, _P, ctypes.c_longlong, _I, _I, _P]),
+    "decode_attn_partial": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
+                                 _I, _P, _SZ, _P, _P]),
+    "decode_attn_combine": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
 }
 
 
@@ -289,6 +292,68 @@ def decode_attn_noalloc(q, K, V, seq_lens, out=None, scale=None, num_splits: int
                                         int(num_splits), _ptr(dev_error), _stream(q, stream))
     _check(st, "decode_attn_noalloc")
     return out
+
+
+def decode_attn_partial(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, seq_lens: torch.Tensor,
+                        row_begin: int = 0, row_end: int | None = None,
+                        o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                        scale: float | None = None, num_splits: int = 0,
+                        workspace: torch.Tensor | None = None,
+                        dev_error: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None):
+    """One shard of a sequence-sharded decode (calls ``decode_attn_partial``): the
+    decode of rows [row_begin, row_end) of every sequence (clipped to its length).
+    Returns ``(o, lse)``: the normalised output [B, h_q, d_v] float32 and the
+    natural-log log-sum-exp of those rows' scores [B, h_q] float32 (-inf when a
+    sequence has no rows in the range)."""
+    B, h_q, h_kv, d_k, d_v, n_max = _cache_dims(q, K, V, seq_lens)
+    if row_end is None:
+        row_end = n_max
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    o, _ = _out(o, torch.float32, B, h_q, d_v, q.device)
+    if lse is None:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=q.device)
+    if lse.shape != (B, h_q) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 tensor [B, h_q] on the query's device")
+    lib = load()
+    with _on_device(q):
+        need = workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, q.dtype, num_splits)
+        if workspace is None:
+            workspace = _workspace(q.device, need)
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.decode_attn_partial(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), int(row_begin),
+                                     int(row_end), _ptr(o), _ptr(lse), B, h_q, h_kv, d_k, d_v,
+                                     n_max, float(scale), _DTYPES[q.dtype], int(num_splits),
+                                     _ptr(workspace), nbytes, _ptr(dev_error), _stream(q, stream))
+    _check(st, "decode_attn_partial")
+    return o, lse
+
+
+def decode_attn_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor,
+                        out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+                        out_dtype: torch.dtype | None = None,
+                        stream: torch.cuda.Stream | None = None):
+    """Merge S partial results over disjoint row sets (calls ``decode_attn_combine``):
+    ``o_parts`` [S, B, h_q, d_v] and ``lse_parts`` [S, B, h_q] (float32, natural log,
+    on this GPU).  Returns ``(out, lse_out)``."""
+    if o_parts.dim() != 4 or lse_parts.dim() != 3 or o_parts.shape[:3] != lse_parts.shape:
+        raise ValueError("expected o_parts [S, B, h_q, d_v] and lse_parts [S, B, h_q]")
+    for name, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    S, B, h_q, d_v = o_parts.shape
+    out, oflag = _out(out, out_dtype, B, h_q, d_v, o_parts.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, h_q), dtype=torch.float32, device=o_parts.device)
+    if lse_out.shape != (B, h_q) or lse_out.dtype != torch.float32 or not lse_out.is_contiguous():
+        raise ValueError("lse_out must be a contiguous float32 tensor [B, h_q]")
+    with _on_device(o_parts):
+        st = load().decode_attn_combine(_ptr(o_parts), _ptr(lse_parts), S, _ptr(out), _ptr(lse_out),
+                                        B, h_q, d_v, DA_FP32 | oflag, _stream(o_parts, stream))
+    _check(st, "decode_attn_combine")
+    return out, lse_out
 
 
 def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, K: torch.Tensor, V: torch.Tensor,

@@ -19,6 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdecode_attn.so")
 INCLUDE = os.path.join(ROOT, "include")
+# The same sources built with DA_TEST_HOOKS: short wait limits and a switch
+# that makes one producer withhold a stage.  Only the tests load it.
+BUILD_TEST = os.path.join(PKG, "_build_test")
+LIB_TEST = os.path.join(PKG, "libdecode_attn_test.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -42,18 +46,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_info: bool = False, test_hooks: bool = False) -> str:
+    """Build the library (``test_hooks``: the test-only variant) and return its path."""
+    build_dir, lib = (BUILD_TEST, LIB_TEST) if test_hooks else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = _headers()
     nvcc = _nvcc()
     jobs = []
     objects = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objects.append(obj)
         if ptxas_info or _stale(obj, [src, *headers]):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *(["-DDA_TEST_HOOKS"] if test_hooks else []), "-c",
+                   src, "-o", obj]
             if ptxas_info:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)
@@ -71,16 +78,16 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError(f"nvcc failed for: {failed}")
-    if jobs or _stale(LIB, objects):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if jobs or _stale(lib, objects):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objects, "-lcudart_static", "-lrt", "-ldl",
                "-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             raise RuntimeError("link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

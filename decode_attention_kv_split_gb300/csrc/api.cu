@@ -15,6 +15,9 @@ using da::KernelShape;
 using da::SplitParams;
 
 std::atomic<uint64_t> g_launches{0};
+#ifdef DA_TEST_HOOKS
+std::atomic<int> g_test_withhold_cta{-1};  // test builds: see decode_attn_test_withhold
+#endif
 thread_local char g_last_cuda_error[256] = "";
 
 int fail_cuda(cudaError_t e, const char* what) {
@@ -342,7 +345,8 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
                       float scale, int dtype_arg, int num_splits, void* workspace,
                       size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream,
                       const void* k_new, const void* v_new, int32_t* seq_lens_out,
-                      const QuantArgs* qa) {
+                      const QuantArgs* qa, int row_off = 0, int row_lim = 0x7fffffff,
+                      float* lse_out = nullptr) {
   if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
   int st = check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype_arg);
   if (st != DA_OK) return st;
@@ -354,6 +358,9 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
   if (qa && (!qa->k_scale || !qa->v_scale || (k_new && (!qa->k_new_scale || !qa->v_new_scale))))
     return DA_ERR_NULL;
   if (qa && (!aligned16(qa->k_scale) || !aligned16(qa->v_scale))) return DA_ERR_ALIGN;
+  // a row range starts the 8-bit row-scale tiles off their 16-byte grid
+  if (qa && row_off != 0) return DA_ERR_UNSUPPORTED;
+  if (k_new && (row_off != 0 || row_lim < n_max)) return DA_ERR_SHAPE;
   if (!isfinite(scale)) return DA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) ||
       (workspace && !aligned16(workspace)))
@@ -387,6 +394,9 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.seq_lens = seq_lens + b0;
     p.out = static_cast<char*>(out) + size_t(b0) * h_q * d_v * out_es;
     p.out_bf16 = dta.out_bf16 ? 1 : 0;
+    p.row_off = row_off;
+    p.row_lim = row_lim;
+    p.lse_out = lse_out ? lse_out + size_t(b0) * h_q : nullptr;
     p.o_part = wl.total ? reinterpret_cast<float*>(ws + wl.o_part) : nullptr;
     p.lse_part = wl.total ? reinterpret_cast<float*>(ws + wl.lse_part) : nullptr;
     p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
@@ -415,6 +425,9 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.max_splits = pl.max_splits;
     p.cta_speed = pl.ks.cta_speed;
     p.scale_log2 = float(double(scale) * 1.4426950408889634);  // log2(e) = 1 / ln 2
+#ifdef DA_TEST_HOOKS
+    p.withhold_cta = b0 == 0 ? g_test_withhold_cta.load() : -1;
+#endif
     const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
     const int grid = int(items < sms ? items : sms);
     cudaError_t err =
@@ -425,9 +438,7 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
     if (wl.total) {
-      err = da::launch_combine(p.o_part, p.lse_part, p.chunk_out, p.seq_lens, p.append, p.out,
-                               p.out_bf16, bn, h_q, d_v, pl.max_splits, n_max, p.unit_nv, h_kv,
-                               pl.head_chunks, pl.ks.heads_per_cta, stream);
+      err = da::launch_combine(p, d_v, pl.ks.heads_per_cta, stream);
       if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
       g_launches.fetch_add(1);
     }
@@ -458,6 +469,17 @@ const char* decode_attn_status_string(int status) {
 const char* decode_attn_last_cuda_error(void) { return g_last_cuda_error; }
 
 uint64_t decode_attn_launch_count(void) { return g_launches.load(); }
+
+#ifdef DA_TEST_HOOKS
+// Test builds only (not part of the product library or its header): from the
+// next decode call on, the producer of split-kernel CTA `cta` never fills the
+// last pipeline stage of its first work item, so that a consumer's bounded
+// wait runs out (2 ms in test builds) and the kernel takes its timeout path.
+// -1 turns it off.
+__attribute__((visibility("default"))) void decode_attn_test_withhold(int cta) {
+  g_test_withhold_cta.store(cta);
+}
+#endif
 
 int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype,
                                int num_splits) {
@@ -502,6 +524,39 @@ int decode_attn_append(const void* q, const void* k_new, const void* v_new, void
   return run_decode(q, K, V, seq_lens, out, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
                     num_splits, workspace, workspace_bytes, dev_error, stream, k_new, v_new,
                     seq_lens_out, nullptr);
+}
+
+int decode_attn_partial(const void* q, const void* K, const void* V, const int32_t* seq_lens,
+                        int row_begin, int row_end, float* o, float* lse, int B, int h_q,
+                        int h_kv, int d_k, int d_v, int n_max, float scale, int dtype,
+                        int num_splits, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_error, cudaStream_t stream) {
+  if (!lse) return DA_ERR_NULL;
+  if ((dtype & DA_OUT_BF16) != 0) return DA_ERR_DTYPE;  // partials are float32
+  if (row_begin < 0 || row_end < row_begin) return DA_ERR_SHAPE;
+  return run_decode(q, K, V, seq_lens, o, B, h_q, h_kv, d_k, d_v, n_max, scale, dtype,
+                    num_splits, workspace, workspace_bytes, dev_error, stream, nullptr, nullptr,
+                    nullptr, nullptr, row_begin, row_end, lse);
+}
+
+int decode_attn_combine(const float* o_parts, const float* lse_parts, int S, void* out,
+                        float* lse_out, int B, int h_q, int d_v, int out_dtype,
+                        cudaStream_t stream) {
+  if (S < 0 || B <= 0 || h_q <= 0) return DA_ERR_SHAPE;
+  if (!out || (S > 0 && (!o_parts || !lse_parts))) return DA_ERR_NULL;  // S = 0 reads neither
+  if (d_v != 64 && d_v != 128 && d_v != 256) return DA_ERR_UNSUPPORTED;
+  if (out_dtype != DA_FP32 && out_dtype != (DA_FP32 | DA_OUT_BF16)) return DA_ERR_DTYPE;
+  const long long heads = (long long)B * h_q;
+  if (heads > (1LL << 36) || (long long)S * heads * d_v > (1LL << 46)) return DA_ERR_SHAPE;
+  if (!aligned16(o_parts) || !aligned16(out)) return DA_ERR_ALIGN;
+  int dev, sms;
+  int st = current_device(&dev, &sms);
+  if (st != DA_OK) return st;
+  cudaError_t e = da::launch_lse_merge(o_parts, lse_parts, S, out, (out_dtype & DA_OUT_BF16) ? 1 : 0,
+                                       lse_out, heads, d_v, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "lse merge launch");
+  g_launches.fetch_add(1);
+  return DA_OK;
 }
 
 int decode_attn(const void* q, const void* K, const void* V, const int32_t* seq_lens, void* out,

@@ -33,11 +33,7 @@ constexpr int kCombineSmemBytes = 96 * 1024;
 
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
-    lse_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                       const int* __restrict__ chunk_in, const int32_t* __restrict__ seq_lens,
-                       int append, void* __restrict__ out, int out_bf16, int h_q, int max_splits,
-                       int n_max, const int* __restrict__ unit_nv, int h_kv, int head_chunks,
-                       int heads_per_cta) {
+    lse_combine_kernel(const SplitParams p, int heads_per_cta) {
   constexpr int EPL = D / 32;
   constexpr int kWarps = kCombineWarps;
   extern __shared__ float csm[];
@@ -50,26 +46,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   // as these CTAs exit and waits for the grid to complete.
   wait_for_prerequisite_grid();
 
+  const int h_q = p.h_q;
   const int bh = blockIdx.x;
   const int b = bh / h_q;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int n = __ldg(seq_lens + b);
-  const bool appended = append && n >= 0 && n < n_max;  // same rule as the split kernel
-  n = n < 0 ? 0 : (n > n_max ? n_max : n);
+  // the rows the split kernel decoded for sequence b (same rules as its work list)
+  int n = __ldg(p.seq_lens + b);
+  const bool appended = p.append && n >= 0 && n < p.n_max;
+  n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
   if (appended) ++n;
-  const int chunk = *reinterpret_cast<const volatile int*>(chunk_in);
+  else n = max(0, min(n, p.row_lim) - p.row_off);
+  const int chunk = *reinterpret_cast<const volatile int*>(p.chunk_out);
   int nv;
   if (chunk > 0) {  // chunked list: ceil(n / chunk) splits
     nv = n <= 0 ? 1 : (n + chunk - 1) / chunk;
   } else {          // balanced list: the unit's count, written by its first CTA
-    const int group = h_q / h_kv, h = bh - b * h_q;
+    const int group = h_q / p.h_kv, h = bh - b * h_q;
     const int kvh = h / group, hc = (h - kvh * group) / heads_per_cta;
-    nv = __ldcg(unit_nv + (b * h_kv + kvh) * head_chunks + hc);
+    nv = __ldcg(p.unit_nv + (b * p.h_kv + kvh) * p.head_chunks + hc);
   }
   if (nv <= 1) return;  // written by the split kernel
-  const float* lse = lse_part + size_t(bh) * max_splits;
-  const float* op = o_part + size_t(bh) * max_splits * D + lane * EPL;
+  const float* lse = p.lse_part + size_t(bh) * p.max_splits;
+  const float* op = p.o_part + size_t(bh) * p.max_splits * D + lane * EPL;
 
   float m = -INFINITY, wsum = 0.f, acc[EPL];
 #pragma unroll
@@ -119,42 +118,104 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
       a += f * red_acc[w * D + d];
     }
     const float v = W > 0.f ? a / W : 0.f;
-    if (out_bf16) static_cast<__nv_bfloat16*>(out)[size_t(bh) * D + d] = __float2bfloat16_rn(v);
-    else static_cast<float*>(out)[size_t(bh) * D + d] = v;
+    if (p.out_bf16) static_cast<__nv_bfloat16*>(p.out)[size_t(bh) * D + d] = __float2bfloat16_rn(v);
+    else static_cast<float*>(p.out)[size_t(bh) * D + d] = v;
+    if (d == 0 && p.lse_out) p.lse_out[bh] = W > 0.f ? (M_use + log2f(W)) * kLn2 : -INFINITY;
   }
 }
 
 template <int D>
-static cudaError_t launch_combine_d(const float* o_part, const float* lse_part,
-                                    const int* chunk_in, const int32_t* seq_lens, int append,
-                                    void* out, int out_bf16, int B, int h_q, int max_splits, int n_max,
-                                    const int* unit_nv, int h_kv, int head_chunks,
-                                    int heads_per_cta, cudaStream_t stream) {
+static cudaError_t launch_combine_d(const SplitParams& p, int heads_per_cta, cudaStream_t stream) {
   static_assert(kCombineWarps * (D + 2) * 4 <= kCombineSmemBytes, "combine scratch");
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(lse_combine_kernel<D>, kCombineSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_dependent(lse_combine_kernel<D>, B * h_q, kCombineWarps * 32,
-                          size_t(kCombineSmemBytes), stream, o_part, lse_part, chunk_in, seq_lens,
-                          append, out, out_bf16, h_q, max_splits, n_max, unit_nv, h_kv,
-                          head_chunks, heads_per_cta);
+  return launch_dependent(lse_combine_kernel<D>, p.B * p.h_q, kCombineWarps * 32,
+                          size_t(kCombineSmemBytes), stream, p, heads_per_cta);
 }
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, int append, void* out, int out_bf16, int B,
-                           int h_q, int d, int max_splits, int n_max, const int* unit_nv, int h_kv,
-                           int head_chunks, int heads_per_cta, cudaStream_t stream) {
+cudaError_t launch_combine(const SplitParams& p, int d, int heads_per_cta, cudaStream_t stream) {
+  if (d == 256) return launch_combine_d<256>(p, heads_per_cta, stream);
+  if (d == 128) return launch_combine_d<128>(p, heads_per_cta, stream);
+  return launch_combine_d<64>(p, heads_per_cta, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Merge of S caller-gathered partials (the exchange step of a sequence-sharded
+// decode).  Part s of head i holds the normalised output o_s of its rows and
+// lse_s, the natural log of its softmax denominator; with L = max_s lse_s,
+//     out = sum_s e^(lse_s - L) o_s / sum_s e^(lse_s - L),
+//     lse = L + log(sum_s e^(lse_s - L)),
+// the same identity as above in the natural-log domain.  One warp per head;
+// each lane holds D/32 consecutive columns and walks the parts in order, with
+// a running maximum (an online merge, four parts in flight).
+// ---------------------------------------------------------------------------
+constexpr int kMergeWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int S,
+                     void* __restrict__ out, int out_bf16, float* __restrict__ lse_out,
+                     long long heads) {
+  constexpr int EPL = D / 32;
+  constexpr float kLog2e = 1.44269504088896341f;
+  wait_for_prerequisite_grid();
+  const long long i = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  if (i >= heads) return;
+  const int lane = threadIdx.x & 31;
+  const float* op = o_parts + i * D + lane * EPL;
+  float m = -INFINITY, wsum = 0.f, acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  for (int s = 0; s < S; s += 4) {
+    float l[4], v[4][EPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = s + u < S;
+      l[u] = ok ? __ldcg(lse_parts + (long long)(s + u) * heads + i) * kLog2e : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        v[u][e] = ok ? __ldcg(op + (long long)(s + u) * heads * D + e) : 0.f;
+    }
+    const float mx = fmaxf(fmaxf(m, fmaxf(l[0], l[1])), fmaxf(l[2], l[3]));
+    const float m_use = mx == -INFINITY ? 0.f : mx;
+    const float scale = ex2(m - m_use);
+    wsum *= scale;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] *= scale;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float f = ex2(l[u] - m_use);
+      wsum += f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(f, v[u][e], acc[e]);
+    }
+    m = mx;
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const long long idx = i * D + lane * EPL + e;
+    const float val = acc[e] * inv;
+    if (out_bf16) static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(val);
+    else static_cast<float*>(out)[idx] = val;
+  }
+  if (lane == 0 && lse_out)
+    lse_out[i] = wsum > 0.f ? (m + log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, void* out,
+                             int out_bf16, float* lse_out, long long heads, int d,
+                             cudaStream_t stream) {
+  const long long grid = (heads + kMergeWarps - 1) / kMergeWarps;
   if (d == 256)
-    return launch_combine_d<256>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
-                                 h_q, max_splits, n_max, unit_nv, h_kv, head_chunks,
-                                 heads_per_cta, stream);
+    return launch_dependent(lse_merge_kernel<256>, int(grid), kMergeWarps * 32, 0, stream, o_parts,
+                            lse_parts, S, out, out_bf16, lse_out, heads);
   if (d == 128)
-    return launch_combine_d<128>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B,
-                                 h_q, max_splits, n_max, unit_nv, h_kv, head_chunks,
-                                 heads_per_cta, stream);
-  return launch_combine_d<64>(o_part, lse_part, chunk_in, seq_lens, append, out, out_bf16, B, h_q,
-                              max_splits, n_max, unit_nv, h_kv, head_chunks, heads_per_cta,
-                              stream);
+    return launch_dependent(lse_merge_kernel<128>, int(grid), kMergeWarps * 32, 0, stream, o_parts,
+                            lse_parts, S, out, out_bf16, lse_out, heads);
+  return launch_dependent(lse_merge_kernel<64>, int(grid), kMergeWarps * 32, 0, stream, o_parts,
+                          lse_parts, S, out, out_bf16, lse_out, heads);
 }
 
 }  // namespace da

@@ -47,6 +47,10 @@ struct SplitParams {
   const float* v_new_scale;
   int append;
   int out_bf16;                  // out holds bf16 (rounded once from the fp32 result)
+  // Rows decoded per sequence: [row_off, min(row_lim, seq_lens[b])) (row_off = 0
+  // and row_lim >= n_max decode every cached row).  Never combined with append.
+  int row_off, row_lim;
+  float* lse_out;                // nullable: [B, h_q] natural-log log-sum-exp of the decoded rows
   int B, h_q, h_kv, group;       // group = h_q / h_kv
   int b_offset;                  // first sequence of this launch inside the tensor maps
   int n_max;
@@ -58,12 +62,36 @@ struct SplitParams {
   int max_splits;                // partial slots per query head (ceil(n_max / chunk))
   float cta_speed;               // one CTA's streaming rate / its even share (split-length model)
   float scale_log2;              // scale * log2(e)
+#ifdef DA_TEST_HOOKS
+  int withhold_cta;              // test builds: this CTA's producer never fills the last stage
+                                 // of its first item (-1: none), so a wait must run out
+#endif
 };
 
 // Wall-clock limit for any wait inside a kernel.  A pipeline wait that has
 // not completed after this long means a copy never landed; the kernel then
-// records DA_DEVERR_TIMEOUT and finishes without waiting further.
+// records DA_DEVERR_TIMEOUT and finishes without waiting further.  Test
+// builds (DA_TEST_HOOKS) give up after 2 ms so that a test can make a wait
+// run out quickly.
+#ifdef DA_TEST_HOOKS
+constexpr unsigned long long kWaitTimeoutNs = 2ull * 1000ull * 1000ull;
+#else
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;
+#endif
+
+// Test builds only: whether this CTA's producer withholds stage t of its k-th
+// item (the last stage of its first item of the CTA the test names).
+__device__ __forceinline__ bool test_withhold(const SplitParams& p, int k, int t, int tiles) {
+#ifdef DA_TEST_HOOKS
+  return int(blockIdx.x) == p.withhold_cta && k == 0 && t == tiles - 1;
+#else
+  (void)p, (void)k, (void)t, (void)tiles;
+  return false;
+#endif
+}
+
+// ln 2: converts a log2-domain log-sum-exp to the natural log.
+constexpr float kLn2 = 0.693147180559945309f;
 
 // ---------------------------------------------------------------------------
 // Small PTX wrappers.
@@ -246,10 +274,10 @@ cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const
                               int d_k, int d_v, int grid, cudaStream_t stream);
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
-cudaError_t launch_combine(const float* o_part, const float* lse_part, const int* chunk_in,
-                           const int32_t* seq_lens, int append, void* out, int out_bf16, int B,
-                           int h_q, int d, int max_splits, int n_max, const int* unit_nv, int h_kv,
-                           int head_chunks, int heads_per_cta, cudaStream_t stream);
+cudaError_t launch_combine(const SplitParams& p, int d, int heads_per_cta, cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, void* out,
+                             int out_bf16, float* lse_out, long long heads, int d,
+                             cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void* V,
                              const int32_t* pos, int B, int h_kv, int row_bytes_k,
                              int row_bytes_v, int n_max, const float* ks_new, const float* vs_new,
@@ -330,6 +358,8 @@ __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedu
   it.row_end = end < n ? end : n;
   if (it.row_end < it.row_begin) it.row_end = it.row_begin;
   it.tiles = (it.row_end - it.row_begin + TILE - 1) / TILE;
+  it.row_begin += p.row_off;  // rows counted from the start of the decoded range
+  it.row_end += p.row_off;
   return it;
 }
 
@@ -401,6 +431,8 @@ __device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, i
   const int last = (s.lens(b) & kAppendFlag) ? n - 1 : -1;
   it.new_row = (last >= it.row_begin && last < it.row_end) ? last : -1;
   it.tiles = (it.row_end - it.row_begin + TILE - 1) / TILE;
+  it.row_begin += p.row_off;  // rows counted from the start of the decoded range
+  it.row_end += p.row_off;
   return it;
 }
 
@@ -531,10 +563,14 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
       n = n < 0 ? 0 : p.n_max;
     }
     if (app) ++n;
+    if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n;
+    if (!app) {  // rows of the decoded range (all of them unless a range was asked for)
+      n = min(n, p.row_lim) - p.row_off;
+      n = n < 0 ? 0 : n;
+    }
     lens[b] = app ? (n | kAppendFlag) : n;
     rows += float(n);
     nmax = n > nmax ? n : nmax;
-    if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n;
   }
   if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
   if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
@@ -716,8 +752,11 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
         const float val = L > 0.f ? __fdividef(sum, L) : 0.f;
         if (single) store_out(p, base + h * stride + d, val);
         else p.o_part[base + h * stride + d] = val;
-        if (!single && d == 0)
-          p.lse_part[(bh0 + h) * p.max_splits + it.split] = L > 0.f ? M + log2f(L) : -INFINITY;
+        if (d == 0) {
+          const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
+          if (!single) p.lse_part[(bh0 + h) * p.max_splits + it.split] = lse2;
+          else if (p.lse_out) p.lse_out[bh0 + h] = lse2 * kLn2;
+        }
       }
     }
   }
@@ -822,6 +861,13 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
         flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
         aborted = true;
         break;
+      }
+      if (test_withhold(p, k, t, it.tiles)) {  // never filled: its consumers' wait runs out
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        continue;
       }
       const uint32_t bar = full0 + 8 * stage;
       const int y0 = it.row_begin + t * TILE;

@@ -212,7 +212,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
 
-      if (!*abort_flag && key0 < valid) {
+      // warp-uniform (the MMAs and shuffles below need the whole warp)
+      const bool live = __all_sync(0xffffffffu, !*abort_flag);
+      if (live && key0 < valid) {
         // ---- Step I: scores for KBW blocks of 16 rows.
         float s[KBW][NB][4];
 #pragma unroll

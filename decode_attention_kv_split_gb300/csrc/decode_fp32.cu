@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         named_bar_sync(2, Cfg::kConsumerThreads);
       }
 
-      if (!*abort_flag && nrows > 0) {
+      // warp-uniform (the shuffles below need the whole warp)
+      const bool live = __all_sync(0xffffffffu, !*abort_flag);
+      if (live && nrows > 0) {
         // Step I: s[g][r] = (scale*log2e*q_g) . K_row, reduced across the warp.
         float s[G][RPW];
 #pragma unroll

@@ -162,6 +162,13 @@ __device__ __forceinline__ void produce_q8(const CUtensorMap* tmK, const CUtenso
         aborted = true;
         break;
       }
+      if (test_withhold(p, k, t, it.tiles)) {  // test builds only: never filled
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        continue;
+      }
       const uint32_t bar = full0 + 8 * stage;
       const int y0 = it.row_begin + t * T;
       const bool with_new = it.new_row >= y0 && it.new_row < y0 + T;
@@ -414,7 +421,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         phase ^= 1u;
       }
 
-      if (!*abort_flag && key0 < valid) {
+      // warp-uniform (the MMAs and shuffles below need the whole warp)
+      const bool live = __all_sync(0xffffffffu, !*abort_flag);
+      if (live && key0 < valid) {
         const uint32_t kbase = smem_u32(kf16);
         const uint32_t vbase = smem_u32(vf16);
         // ---- Step I: scores for KBW blocks of 16 rows

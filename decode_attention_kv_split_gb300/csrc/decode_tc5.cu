@@ -185,7 +185,8 @@ template <int T, int NSLOT, int TILE_BYTES, int HALF_BYTES, int ROW_BYTES>
 __device__ __forceinline__ void produce_ring(const CUtensorMap* map, const void* new_rows,
                                              const SplitParams& p, const Schedule& s,
                                              uint32_t slots, uint32_t newslots, uint32_t full0,
-                                             uint32_t empty0, volatile int* abort_flag) {
+                                             uint32_t empty0, volatile int* abort_flag,
+                                             bool may_withhold) {
   prefetch_tmap(map);
   const uint64_t policy = l2_policy_evict_first();
   int slot = 0;
@@ -200,6 +201,13 @@ __device__ __forceinline__ void produce_ring(const CUtensorMap* map, const void*
         flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
         aborted = true;
         break;
+      }
+      if (may_withhold && test_withhold(p, k, t, it.tiles)) {  // test builds only
+        if (++slot == NSLOT) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        continue;
       }
       const uint32_t bar = full0 + 8 * slot;
       const int y0 = it.row_begin + t * T;
@@ -305,10 +313,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == 8) {
     if (lane == 0)
       produce_ring<T, KST, Cfg::kTileBytes, Cfg::kHalfBytes, Cfg::kRowBytes>(
-          &tmK, p.k_new, p, sched, smem_u32(kslots), smem_u32(knew), kfull0, kempty0, abort_flag);
+          &tmK, p.k_new, p, sched, smem_u32(kslots), smem_u32(knew), kfull0, kempty0, abort_flag,
+          true);
     else if (lane == 1)
       produce_ring<T, VST, Cfg::kTileBytes, Cfg::kHalfBytes, Cfg::kRowBytes>(
-          &tmV, p.v_new, p, sched, smem_u32(vslots), smem_u32(vnew), vfull0, vempty0, abort_flag);
+          &tmV, p.v_new, p, sched, smem_u32(vslots), smem_u32(vnew), vfull0, vempty0, abort_flag,
+          false);
     return;
   }
 
@@ -530,7 +540,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       tc5::fence_after();
-      const bool live = !*abort_flag;
+      // warp-uniform: the TMEM loads below are .sync.aligned
+      const bool live = __all_sync(0xffffffffu, !*abort_flag);
       const int valid = min(T, it.row_end - (it.row_begin + t * T));
       const bool row_ok = t_row < valid;
       float s[HT];
@@ -643,7 +654,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       inv_l[h] = L[h] > 0.f ? __fdividef(1.f, L[h]) : 0.f;
     }
     float o[HT];
-    if (it.tiles > 0 && !*abort_flag) {
+    const bool epi_live = __all_sync(0xffffffffu, !*abort_flag);  // warp-uniform, as above
+    if (it.tiles > 0 && epi_live) {
       // O^T = (even chain head + remainder) + (odd chain head + remainder)
       float r1[HT];
       tc5::ld16x(o_col + hb + lane_base, o, HT);
@@ -674,7 +686,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (single) store_out(p, base + h * stride, o[h] * inv_l[h]);
           else p.o_part[base + h * stride] = o[h] * inv_l[h];
         }
-      if (!single && quarter == 0 && lane < HT && hb + lane < nheads) {
+      if ((!single || p.lse_out) && quarter == 0 && lane < HT && hb + lane < nheads) {
         float m_h = m_run[0], l_h = L[0];
 #pragma unroll
         for (int h = 1; h < HT; ++h)
@@ -682,8 +694,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             m_h = m_run[h];
             l_h = L[h];
           }
-        p.lse_part[(bh0 + hb + lane) * p.max_splits + it.split] =
-            l_h > 0.f ? m_h + log2f(l_h) : -INFINITY;
+        const float lse2 = l_h > 0.f ? m_h + log2f(l_h) : -INFINITY;
+        if (!single) p.lse_part[(bh0 + hb + lane) * p.max_splits + it.split] = lse2;
+        else p.lse_out[bh0 + hb + lane] = lse2 * kLn2;
       }
     }
     // the next item's first P.V overwrites O: our TMEM reads are complete

@@ -215,6 +215,52 @@ DA_API int decode_attn_noalloc(const void* q, const void* K, const void* V, cons
                                cudaStream_t stream);
 
 /*
+ * Sequence-sharded decode, the per-shard half.  When the cached rows of a
+ * sequence are spread over several GPUs (or several row ranges of one
+ * cache), each holder decodes its own rows and the exact softmax over all of
+ * them is recovered by a log-sum-exp merge of the per-holder results ("Phase
+ * 3, Section 6: StoryLM-0 head-parallel attention" shards attention across
+ * devices and gathers the shards; split by rows, the gather is this merge).
+ * For every b and query head h, with n = seq_lens[b] and the rows
+ * R_b = [min(row_begin, n), min(row_end, n)):
+ *   o[b,h,:]  = sum_{l in R_b} a_l V[b,kv,l,:], a the softmax of Steps I-II
+ *               of decode_attn_ex taken over R_b only (normalised);
+ *   lse[b,h]  = log sum_{l in R_b} exp(s_l), natural log, s_l the scaled
+ *               scores of Step I;
+ *   an empty R_b gives o = 0 and lse = -inf.
+ *   o   : device float32 [B, h_q, d_v]      lse : device float32 [B, h_q]
+ *   row_begin, row_end : 0 <= row_begin <= row_end; rows past n are ignored.
+ * dtype is DA_FP32 or DA_BF16 (no DA_OUT_BF16: partials stay float32);
+ * other arguments, workspace and errors as decode_attn_ex (the workspace size
+ * is decode_attn_workspace_bytes of the same request).
+ */
+DA_API int decode_attn_partial(const void* q, const void* K, const void* V,
+                               const int32_t* seq_lens, int row_begin, int row_end, float* o,
+                               float* lse, int B, int h_q, int h_kv, int d_k, int d_v, int n_max,
+                               float scale, int dtype, int num_splits, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_error, cudaStream_t stream);
+
+/*
+ * Sequence-sharded decode, the merge half: combines S partial results over
+ * disjoint row sets, as produced by decode_attn_partial and gathered by the
+ * caller into this GPU's own memory (a partial is never read from a peer):
+ *   L = max_s lse_s;  out = sum_s e^(lse_s - L) o_s / sum_s e^(lse_s - L);
+ *   lse_out = L + log(sum_s e^(lse_s - L))      (-inf and out = 0 when every
+ *   part is empty), which equals the decode over the union of the rows.
+ *   o_parts   : device float32 [S, B, h_q, d_v], 16-byte aligned
+ *   lse_parts : device float32 [S, B, h_q], natural log
+ *   out       : device [B, h_q, d_v], float32, or bf16 when out_dtype is
+ *               DA_FP32 | DA_OUT_BF16; 16-byte aligned
+ *   lse_out   : nullable device float32 [B, h_q]
+ *   d_v in {64, 128, 256}; S >= 0 (S = 0 gives out = 0, lse_out = -inf, and
+ *   o_parts / lse_parts may then be NULL).
+ * One kernel launch on `stream`.
+ */
+DA_API int decode_attn_combine(const float* o_parts, const float* lse_parts, int S, void* out,
+                               float* lse_out, int B, int h_q, int d_v, int out_dtype,
+                               cudaStream_t stream);
+
+/*
  * KV-cache accumulation ("MoA-Structured Decode Attention", introduction
  * item 3, with the gamma offsets of section 3): for every b < B, h < h_kv
  *   K[b, h, pos[b], :] = k_new[b, h, :]     (d_k elements)

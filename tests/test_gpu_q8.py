@@ -227,3 +227,38 @@ def test_q8_fused_append_decode(o, kind, case, splits):
     assert (int(err.item()) == api.DEVERR_POS) == (skipped > 0)
     want = oracle_decode_q8(o, k, q, kc, ks, vc, vs, new_lens, w.scale)
     _check(out.cpu(), want, TOL)
+
+
+# ----------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name", ["gqa_llama3_8b_fp8", "gqa_llama3_8b_int8", "long_llama2_70b_fp8"])
+def test_q8_full_size_workload_every_head(o, name):
+    """The bench's 8-bit workloads at full size (ragged GQA in balanced pieces; the
+    131072-row long context with the library's splits): the oracle quantizes the
+    seeded values, the GPU decodes the codes, every head is compared."""
+    w = W.WORKLOADS[name]
+    k = 1 if w.dtype == torch.int8 else 2
+    K, V = W.cache(w)
+    kc, ks = o.quantize(K.numpy(), k)
+    vc, vs = o.quantize(V.numpy(), k)
+    del K, V
+    lens = W.seq_lens(w)
+    for b, n in enumerate(lens.tolist()):
+        kc[b, :, n:] = 0x7F
+        vc[b, :, n:] = 0x7F
+        ks[b, :, n:] = np.nan
+        vs[b, :, n:] = np.nan
+    q = W.query(w)
+    dev = torch.device("cuda")
+    out = api.decode_attn_q8(q.to(dev), _codes_tensor(kc, w.dtype).to(dev),
+                             _codes_tensor(vc, w.dtype).to(dev), torch.from_numpy(ks).to(dev),
+                             torch.from_numpy(vs).to(dev), lens.to(dev), num_splits=w.num_splits)
+    torch.cuda.synchronize()
+    Kd = o.dequant(kc, ks, k)
+    Vd = o.dequant(vc, vs, k)
+    del kc, vc
+    for b, n in enumerate(lens.tolist()):
+        Kd[b, :, n:] = 0.0
+        Vd[b, :, n:] = 0.0
+    want, _ = o.decode(q.float().numpy(), Kd.astype(np.float32), Vd.astype(np.float32),
+                       lens.numpy(), w.scale, threads=max(1, o.max_threads()))
+    _check(out.cpu(), want, TOL)

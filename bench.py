@@ -548,7 +548,7 @@ def run_ours(args, w, world, rank, local):
     if h.n_rot * h.kv_touch < 4 * L2_BYTES:
         bytes_str += " (L2-resident)"
 
-    cpu = oracle_baseline(w, args.cpu_seconds)
+    cpu = oracle_baseline(w, args.cpu_seconds) if args.cpu_seconds > 0 else None
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

@@ -19,7 +19,7 @@
 namespace da {
 
 // One CTA of 16 warps per (b, query head).  Warp w merges splits w, w+16,
-// ... in one pass, four in flight, keeping a running maximum of the lse
+// ... in one pass, 16 in flight, keeping a running maximum of the lse
 // values it has seen (the online form of the combine; every weight is taken
 // against the same maximum that scales the warp's sum).  Each lane holds D/32
 // consecutive columns.  The 16 warp results meet in shared memory and are
@@ -31,8 +31,23 @@ constexpr int kCombineWarps = 16;
 // drains, and without the cap its CTAs pile up on the first SMs to free up.
 constexpr int kCombineSmemBytes = 96 * 1024;
 
+// EPL consecutive floats (EPL * 4-byte aligned) through L2, as vector loads.
+template <int EPL>
+__device__ __forceinline__ void ldcg_vec(float (&v)[EPL], const float* src) {
+  if constexpr (EPL == 2) {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+    v[0] = x.x, v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; i += 4) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(src + i));
+      v[i] = x.x, v[i + 1] = x.y, v[i + 2] = x.z, v[i + 3] = x.w;
+    }
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineWarps * 32, 2)
     lse_combine_kernel(const SplitParams p, int heads_per_cta) {
   constexpr int EPL = D / 32;
   constexpr int kWarps = kCombineWarps;
@@ -41,9 +56,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   float* red_m = csm + kWarps * D;      // [kWarps]
   float* red_w = red_m + kWarps;        // [kWarps]
 
-  // No early launch_dependents here: a next kernel whose CTAs sat resident
-  // beside these ones, waiting for this grid, slowed the merge.  It launches
-  // as these CTAs exit and waits for the grid to complete.
+  // The next kernel on the stream may launch now: a split kernel's CTAs
+  // cannot share an SM with a combine CTA (registers), so they take the SMs
+  // this grid leaves free and wait there (griddepcontrol.wait) until it has
+  // completed, with their set-up done and no launch latency left.
+  allow_dependent_launch();
   wait_for_prerequisite_grid();
 
   const int h_q = p.h_q;
@@ -70,27 +87,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   const float* lse = p.lse_part + size_t(bh) * p.max_splits;
   const float* op = p.o_part + size_t(bh) * p.max_splits * D + lane * EPL;
 
+  // NB splits per warp in flight at once (vector loads from L2): one pass
+  // covers NB * kWarps splits, 272 for d <= 128 (256 splits and the one that
+  // rows appended past n_max open).
+  constexpr int NB = EPL == 4 ? 17 : (EPL == 2 ? 16 : 8);
   float m = -INFINITY, wsum = 0.f, acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  for (int s = warp; s < nv; s += 4 * kWarps) {
-    float l[4], v[4][EPL];
+  for (int s = warp; s < nv; s += NB * kWarps) {
+    float l[NB], v[NB][EPL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < NB; ++u) {
       const int su = s + u * kWarps;
       const bool ok = su < nv;
       l[u] = ok ? __ldcg(lse + su) : -INFINITY;
+      if (ok) ldcg_vec<EPL>(v[u], op + size_t(su) * D);
+      else {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) v[u][e] = ok ? __ldcg(op + size_t(su) * D + e) : 0.f;
+        for (int e = 0; e < EPL; ++e) v[u][e] = 0.f;
+      }
     }
-    const float mx = fmaxf(fmaxf(m, fmaxf(l[0], l[1])), fmaxf(l[2], l[3]));
+    float mx = m;
+#pragma unroll
+    for (int u = 0; u < NB; ++u) mx = fmaxf(mx, l[u]);
     const float m_use = mx == -INFINITY ? 0.f : mx;  // only empty splits so far
     const float scale = ex2(m - m_use);              // 0 while m is -inf
     wsum *= scale;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] *= scale;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < NB; ++u) {
       const float f = ex2(l[u] - m_use);
       wsum += f;
 #pragma unroll

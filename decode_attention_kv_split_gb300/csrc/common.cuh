@@ -288,10 +288,12 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* K, void
 //
 // Sequence b is cut into nv_b = max(1, ceil(n_b / chunk)) splits of `chunk`
 // rows.  Each (kv head, head chunk) of b is a unit; each (unit, split) is a
-// work item.  Items are numbered sequence by sequence, unit by unit, split by
-// split, so the splits of one unit are consecutive and units complete one
-// after another.  Persistent CTAs take items i = blockIdx.x + k * gridDim.x.
-// Every CTA builds the same list in shared memory from seq_lens.
+// work item.  Items are numbered in two runs: first every split but the last
+// of every unit (sequence by sequence, unit by unit, split by split), then
+// the last split of every unit, which is usually shorter than `chunk`.
+// Persistent CTAs take items i = blockIdx.x + k * gridDim.x, so the full
+// splits are dealt evenly and the short ones fill the last round.  Every CTA
+// builds the same list in shared memory from seq_lens.
 // ---------------------------------------------------------------------------
 // Shared-memory words of the work list: first[] and lens[] of up to
 // kMaxBatchPerLaunch sequences, reduction scratch for up to 16 warps, and the
@@ -307,7 +309,8 @@ constexpr int kSchedWords = kSchedItems + kItemCache * kItemWords;
 
 struct Schedule {
   int* w;           // kSchedWords ints of shared memory:
-                    //   [0, B]      chunked: first item of sequence b (first[B] = total);
+                    //   [0, B]      chunked: first item of sequence b's run of full
+                    //               splits (first[B] = F, the items of that run);
                     //               balanced: stream offset of sequence b's rows per
                     //               unit, sum of max(n, 1) over earlier sequences
                     //   kSchedLens  rows to decode per sequence; bit 31 set when
@@ -335,22 +338,33 @@ struct Item {
 
 template <int TILE>
 __device__ __forceinline__ Item schedule_item(const SplitParams& p, const Schedule& s, int i) {
-  // last b with first[b] <= i
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s.first(mid) <= i) lo = mid; else hi = mid - 1;
-  }
-  Item it;
-  it.b = lo;
   const int per_seq = p.h_kv * p.head_chunks;
-  it.nv = (s.first(lo + 1) - s.first(lo)) / per_seq;
-  const int r = i - s.first(lo);
-  const int unit = r / it.nv;
-  it.split = r - unit * it.nv;
+  const int F = s.first(p.B);
+  Item it;
+  int unit;
+  if (i < F) {  // a full split: last b with first[b] <= i (then first[b + 1] > i)
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s.first(mid) <= i) lo = mid; else hi = mid - 1;
+    }
+    it.b = lo;
+    const int full = (s.first(lo + 1) - s.first(lo)) / per_seq;  // nv - 1
+    it.nv = full + 1;
+    const int r = i - s.first(lo);
+    unit = r / full;
+    it.split = r - unit * full;
+  } else {      // the last split of unit (i - F) % per_seq of sequence (i - F) / per_seq
+    const int j = i - F;
+    it.b = j / per_seq;
+    unit = j - it.b * per_seq;
+    const int n = len_of(s.lens(it.b));
+    it.nv = n <= 0 ? 1 : (n - 1) / s.chunk + 1;
+    it.split = it.nv - 1;
+  }
   it.kvh = unit / p.head_chunks;
   it.hc = unit - it.kvh * p.head_chunks;
-  const int lv = s.lens(lo);
+  const int lv = s.lens(it.b);
   const int n = len_of(lv);
   it.new_row = (lv & kAppendFlag) ? n - 1 : -1;
   it.row_begin = it.split * s.chunk;
@@ -656,7 +670,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
     }
     s.chunk = choose_chunk(p, lens, TILE, gridDim.x, all_rows, all_max, red);
   }
-  // exclusive scan of items per sequence by warp 0
+  // exclusive scan of the full-split items per sequence by warp 0
   if (tid < 32) {
     int carry = 0;
     for (int base = 0; base < p.B; base += 32) {
@@ -664,7 +678,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
       int c = 0;
       if (b < p.B) {
         const int n = len_of(lens[b]);
-        c = per_seq * (n <= 0 ? 1 : (n - 1) / s.chunk + 1);
+        c = per_seq * (n <= 0 ? 0 : (n - 1) / s.chunk);
       }
       int x = c;
 #pragma unroll
@@ -678,7 +692,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
     if (tid == 0) first[p.B] = carry;
   }
   __syncthreads();
-  s.total = first[p.B];
+  s.total = first[p.B] + per_seq * p.B;  // and one last split per unit
   if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = s.chunk;
   // decode this CTA's first items, one per thread
   const int mine = s.total > int(blockIdx.x) ? (s.total - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;

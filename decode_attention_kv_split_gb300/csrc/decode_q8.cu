@@ -542,16 +542,337 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// d = 128: MMA fragments built straight from the code tiles, in registers.
+//
+// The code tiles arrive with the 128-byte swizzle (16-byte chunk c of row r
+// at chunk c ^ (r & 7)), so the reads below are bank-conflict free, and no
+// fp16 copy of a stage is ever written to shared memory.  With lane = 4 g + t:
+//   Step I  (S^T = K . Q^T, rows of K as M): lane (g, t) reads bytes
+//           [32 t, 32 t + 32) of rows g and g + 8 of its 16-row block and
+//           uses the 4 codes at 32 t + 4 kb as the A elements of k-block kb
+//           at logical columns 2t, 2t+1, 2t+8, 2t+9.  This relabels the 128
+//           columns of d one to one, and the B fragments (q) are taken in the
+//           same order, so every score is the same sum of the same products.
+//   Step III (O^T += V^T . P^T, d as M): lane (g, t) reads bytes
+//           [16 g, 16 g + 16) of rows 2t, 2t+1, 2t+8, 2t+9; a byte permute
+//           pairs each column of rows 2t and 2t+1 (the two k elements of an A
+//           register), and m-block mb takes columns 16 g + 2 mb (as row g of
+//           the block) and 16 g + 2 mb + 1 (as row g + 8).  The outputs of
+//           lane (g, t) are then columns [16 g, 16 g + 16) of heads 2t, 2t+1.
+// ---------------------------------------------------------------------------
+template <int STAGES_, int KIND_>
+struct Q8RCfg {
+  static constexpr int D = 128;
+  static constexpr int KW = 8;             // consumer warps, one 16-row block each
+  static constexpr int STAGES = STAGES_;
+  static constexpr int KIND = KIND_;
+  static constexpr int HG = 1;
+  static constexpr int kHPW = 8;
+  static constexpr int kHeadsPerCta = 8;
+  static constexpr int kTile = 16 * KW;
+  static constexpr int kConsumerWarps = KW;
+  static constexpr int kConsumerThreads = 32 * KW;
+  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int kCodeBytes = kTile * D;
+  static constexpr int kScaleBytes = kTile * 4;
+  static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kScaleBytes;
+  static constexpr int kQBytes = kHeadsPerCta * D * 2;
+  static constexpr int kNewBytes = 2 * D;
+  static constexpr int kSlotStride = D + 4;
+  static constexpr int kEpiAccFloats = KW * kHPW * kSlotStride;
+  static constexpr int kEpiMLFloats = 2 * KW * kHPW;
+  static constexpr int kSchedWords = da::kSchedWords;
+  static constexpr size_t kSmemBytes =
+      1024 + size_t(STAGES) * (kStageBytes + kQBytes + kNewBytes) +
+      size_t(kEpiAccFloats + kEpiMLFloats + kSchedWords) * 4 + 2 * STAGES * 8 + 16;
+  static_assert(KIND == 1 || KIND == 2, "code type");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment (128-byte swizzle)");
+  static_assert((kEpiAccFloats + kEpiMLFloats) % 2 == 0, "mbarrier alignment");
+};
+
+// 16 bytes of row `row` of a 128-byte-swizzled code tile, logical chunk `chunk`.
+__device__ __forceinline__ uint4 ld_code_chunk(const uint8_t* tile, int row, int chunk) {
+  return *reinterpret_cast<const uint4*>(tile + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    split_decode_q8r_kernel(const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV,
+                            const __grid_constant__ CUtensorMap tmKs,
+                            const __grid_constant__ CUtensorMap tmVs, const SplitParams p) {
+  constexpr int D = Cfg::D, KW = Cfg::KW, STAGES = Cfg::STAGES, T = Cfg::kTile;
+  constexpr int kHPW = Cfg::kHPW;
+  constexpr int MB = D / 16;   // 16-wide blocks of d (Step III m-blocks; Step I k-blocks)
+  constexpr int KIND = Cfg::KIND;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* qslots = smem + size_t(STAGES) * Cfg::kStageBytes;
+  uint8_t* newslots = qslots + size_t(STAGES) * Cfg::kQBytes;
+  float* epi_acc = reinterpret_cast<float*>(newslots + size_t(STAGES) * Cfg::kNewBytes);
+  float* epi_m = epi_acc + Cfg::kEpiAccFloats;
+  float* epi_l = epi_m + KW * kHPW;
+  int* sched_words = reinterpret_cast<int*>(epi_l + KW * kHPW);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sched_words + Cfg::kSchedWords);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES);
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {  // the tensor maps do not depend on the preceding grid
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmKs);
+    prefetch_tmap(&tmVs);
+  }
+  // Launched as a programmatic dependent: nothing before this line reads
+  // memory that the previous grid on the stream may write.
+  wait_for_prerequisite_grid();
+  const Schedule sched = build_schedule<T>(p, sched_words);
+  allow_dependent_launch();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == KW) {
+    if (lane == 0)
+      produce_q8<Cfg>(&tmK, &tmV, &tmKs, &tmVs, p, sched, ring, smem_u32(qslots),
+                      smem_u32(newslots), full0, empty0, abort_flag);
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int g = lane >> 2;   // MMA fragment row group
+  const int t = lane & 3;    // MMA fragment column pair
+  const int key0 = warp * 16;  // first row of this warp's block inside a stage
+  const int rA = key0 + g, rB = rA + 8;             // Step I rows (and P rows)
+  const int r0 = key0 + 2 * t, r1 = r0 + 1, r2 = r0 + 8, r3 = r0 + 9;  // Step III rows
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int k = 0; k < sched.mine; ++k) {
+    const Item it = cta_item<T>(p, sched, k);
+    const int head_base = it.hc * Cfg::kHeadsPerCta;
+    const size_t kvhead = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
+    uint32_t qf[MB][2];  // B fragments of q (head g), in the permuted column order
+
+    float m_run[2], l_run[2];
+    float acc[MB][4];
+    m_run[0] = m_run[1] = -INFINITY;
+    l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mb][e] = 0.f;
+
+    for (int tt = 0; tt < it.tiles; ++tt) {
+      if (!mbar_wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
+        if (!*abort_flag) {
+          *abort_flag = 1;
+          flag_error(p.dev_error, DA_DEVERR_TIMEOUT);
+        }
+      }
+      const uint8_t* st = smem + size_t(stage) * Cfg::kStageBytes;
+      const uint8_t* ktile = st;
+      const uint8_t* vtile = st + Cfg::kCodeBytes;
+      const float* ks_t = reinterpret_cast<const float*>(st + 2 * Cfg::kCodeBytes);
+      const float* vs_t = ks_t + T;
+      const uint8_t* nslot = newslots + size_t(stage) * Cfg::kNewBytes;
+      const int tile_row0 = it.row_begin + tt * T;
+      const int valid = min(T, it.row_end - tile_row0);
+      const int new_local = (it.new_row >= tile_row0 && it.new_row < tile_row0 + T)
+                                ? it.new_row - tile_row0
+                                : -1;
+
+      // ---- this lane's codes and row scales, into registers
+      uint4 kA0 = ld_code_chunk(ktile, rA, 2 * t), kA1 = ld_code_chunk(ktile, rA, 2 * t + 1);
+      uint4 kB0 = ld_code_chunk(ktile, rB, 2 * t), kB1 = ld_code_chunk(ktile, rB, 2 * t + 1);
+      uint4 v0 = ld_code_chunk(vtile, r0, g), v1 = ld_code_chunk(vtile, r1, g);
+      uint4 v2 = ld_code_chunk(vtile, r2, g), v3 = ld_code_chunk(vtile, r3, g);
+      float skA = ks_t[rA], skB = ks_t[rB], svA = vs_t[rA], svB = vs_t[rB];
+      if (new_local >= key0 && new_local < key0 + 16) {  // warp-uniform: the appended row
+        const uint4* nk = reinterpret_cast<const uint4*>(nslot);
+        const uint4* nv = reinterpret_cast<const uint4*>(nslot + D);
+        const float nks = __ldg(p.k_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+        const float nvs = __ldg(p.v_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+        if (rA == new_local) kA0 = nk[2 * t], kA1 = nk[2 * t + 1], skA = nks, svA = nvs;
+        if (rB == new_local) kB0 = nk[2 * t], kB1 = nk[2 * t + 1], skB = nks, svB = nvs;
+        if (r0 == new_local) v0 = nv[g];
+        if (r1 == new_local) v1 = nv[g];
+        if (r2 == new_local) v2 = nv[g];
+        if (r3 == new_local) v3 = nv[g];
+      }
+      // rows past the end may hold anything: their values must not reach O
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      if (r0 >= valid) v0 = zero;
+      if (r1 >= valid) v1 = zero;
+      if (r2 >= valid) v2 = zero;
+      if (r3 >= valid) v3 = zero;
+      const float fkA = rA < valid ? skA * p.scale_log2 : 0.f;
+      const float fkB = rB < valid ? skB * p.scale_log2 : 0.f;
+      const float fvA = rA < valid ? svA : 0.f;
+      const float fvB = rB < valid ? svB : 0.f;
+      if (tt == 0) {  // q of head g (rows past the group are zero), bf16 -> fp16 B fragments
+        const bool ok = head_base + g < p.group;
+        const uint4* qs = reinterpret_cast<const uint4*>(qslots + size_t(stage) * Cfg::kQBytes +
+                                                         g * (D * 2) + t * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // 8 bf16 values = columns 32t + 8c .. + 7
+          const uint4 w = ok ? qs[c] : zero;
+          qf[2 * c][0] = q8::pack_f16x2(bf16_lo_to_f32(w.x), bf16_hi_to_f32(w.x));
+          qf[2 * c][1] = q8::pack_f16x2(bf16_lo_to_f32(w.y), bf16_hi_to_f32(w.y));
+          qf[2 * c + 1][0] = q8::pack_f16x2(bf16_lo_to_f32(w.z), bf16_hi_to_f32(w.z));
+          qf[2 * c + 1][1] = q8::pack_f16x2(bf16_lo_to_f32(w.w), bf16_hi_to_f32(w.w));
+        }
+      }
+      // the appended row goes into the caches once per kv head, by the warp that owns it
+      if (new_local >= key0 && new_local < key0 + 16 && it.hc == 0 && !*abort_flag) {
+        const size_t row_off = kvhead * size_t(p.n_max) + size_t(it.new_row);
+        if (lane < D / 16) {
+          reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + row_off * D)[lane] =
+              reinterpret_cast<const uint4*>(nslot)[lane];
+          reinterpret_cast<uint4*>(static_cast<char*>(p.v_cache) + row_off * D)[lane] =
+              reinterpret_cast<const uint4*>(nslot + D)[lane];
+        }
+        if (lane == 0) {
+          p.k_scale[row_off] = __ldg(p.k_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+          p.v_scale[row_off] = __ldg(p.v_new_scale + size_t(it.b) * p.h_kv + it.kvh);
+        }
+      }
+      __syncwarp();
+      // every byte this warp needs from the stage is in registers now
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+
+      // warp-uniform (the MMAs and shuffles below need the whole warp)
+      const bool live = __all_sync(0xffffffffu, !*abort_flag);
+      if (live && key0 < valid) {
+        // ---- Step I: two independent accumulation chains over the 8 k-blocks
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kb = 0; kb < MB; ++kb) {
+          uint32_t a[4];
+          q8::codes_to_f16<KIND>(word_of(kb < 4 ? kA0 : kA1, kb & 3), a[0], a[2]);
+          q8::codes_to_f16<KIND>(word_of(kb < 4 ? kB0 : kB1, kb & 3), a[1], a[3]);
+          if (kb & 1) q8::mma_f16_16816(s2, a, qf[kb][0], qf[kb][1]);
+          else q8::mma_f16_16816(s, a, qf[kb][0], qf[kb][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[e] += s2[e];
+        // ---- Step II: scale by the K row scales, mask, running max and sum
+        float alpha[2];
+        bool changed = false;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          s[j] = rA < valid ? s[j] * fkA : -INFINITY;
+          s[j + 2] = rB < valid ? s[j + 2] * fkB : -INFINITY;
+          float mx = fmaxf(s[j], s[j + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[j], mx);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha[j] = ex2(m_run[j] - m_use);
+          changed |= (m_new != m_run[j]);
+          m_run[j] = m_new;
+          s[j] = ex2(s[j] - m_use);
+          s[j + 2] = ex2(s[j + 2] - m_use);
+          l_run[j] = l_run[j] * alpha[j] + (s[j] + s[j + 2]);
+        }
+        if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) {
+            acc[mb][0] *= alpha[0];
+            acc[mb][1] *= alpha[1];
+            acc[mb][2] *= alpha[0];
+            acc[mb][3] *= alpha[1];
+          }
+        }
+        // ---- Step III: O^T += V^T . (P * vs)^T, P as fp16 head + fp16 remainder
+        const float p0 = s[0] * fvA, p1 = s[1] * fvA, p2 = s[2] * fvB, p3 = s[3] * fvB;
+        const uint32_t h0 = q8::pack_f16x2(p0, p1);  // row g
+        const uint32_t h1 = q8::pack_f16x2(p2, p3);  // row g + 8
+        const uint32_t l0 = q8::pack_f16x2(p0 - q8::f16_lo(h0), p1 - q8::f16_hi(h0));
+        const uint32_t l1 = q8::pack_f16x2(p2 - q8::f16_lo(h1), p3 - q8::f16_hi(h1));
+        const uint32_t ph0 = movmatrix_trans(h0), ph1 = movmatrix_trans(h1);
+        const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) {
+          const int w = mb >> 1;
+          const uint32_t sel = (mb & 1) ? 0x7362u : 0x5140u;  // columns 2mb, 2mb+1 of the lane's 16
+          const uint32_t x01 = __byte_perm(word_of(v0, w), word_of(v1, w), sel);
+          const uint32_t x23 = __byte_perm(word_of(v2, w), word_of(v3, w), sel);
+          uint32_t a[4];
+          q8::codes_to_f16<KIND>(x01, a[0], a[1]);  // rows 2t, 2t+1 at columns 2mb (a0), 2mb+1 (a1)
+          q8::codes_to_f16<KIND>(x23, a[2], a[3]);  // rows 2t+8, 2t+9
+          q8::mma_f16_16816(acc[mb], a, ph0, ph1);
+          q8::mma_f16_16816(acc[mb], a, pl0, pl1);
+        }
+      }
+    }
+
+    // ---- Epilogue: per-warp state to shared slots, then the shared finish.
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float v = l_run[j];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l_run[j] = v;
+    }
+    named_bar_sync(1, Cfg::kConsumerThreads);  // earlier readers of the slots are done
+    float* slot = epi_acc + warp * kHPW * Cfg::kSlotStride;
+    if (lane < 4) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        epi_m[warp * kHPW + 2 * lane + j] = m_run[j];
+        epi_l[warp * kHPW + 2 * lane + j] = l_run[j];
+      }
+    }
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+      const int d0 = 16 * g + 2 * mb;  // acc[mb][0..1]: column d0; acc[mb][2..3]: d0 + 1
+      slot[(2 * t) * Cfg::kSlotStride + d0] = acc[mb][0];
+      slot[(2 * t + 1) * Cfg::kSlotStride + d0] = acc[mb][1];
+      slot[(2 * t) * Cfg::kSlotStride + d0 + 1] = acc[mb][2];
+      slot[(2 * t + 1) * Cfg::kSlotStride + d0 + 1] = acc[mb][3];
+    }
+    named_bar_sync(1, Cfg::kConsumerThreads);
+    finish_item<D, 1, KW, kHPW, Cfg::kSlotStride>(p, it, epi_acc, epi_m, epi_l, threadIdx.x,
+                                                  Cfg::kConsumerThreads, abort_flag);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Variants and launcher.
 // ---------------------------------------------------------------------------
 template <int KIND>
-using Q8D128 = Q8Cfg<128, 8, 1, 3, KIND>;
+using Q8D128 = Q8RCfg<5, KIND>;   // register-fragment kernel, 128-byte-swizzled code tiles
 template <int KIND>
 using Q8D64 = Q8Cfg<64, 8, 1, 6, KIND>;
 
 KernelShape q8_shape(int d) {
-  const int tile = d == 128 ? Q8D128<1>::kTile : Q8D64<1>::kTile;
-  return KernelShape{tile, 8, d, 0, 1.0f};
+  if (d == 128) return KernelShape{Q8D128<1>::kTile, 8, 128, 1, 1.0f};
+  return KernelShape{Q8D64<1>::kTile, 8, 64, 0, 1.0f};
 }
 
 template <class Cfg>
@@ -565,12 +886,24 @@ static cudaError_t launch_q8_cfg(const SplitParams& p, const CUtensorMap& tk,
                           stream, tk, tv, tks, tvs, p);
 }
 
+template <class Cfg>
+static cudaError_t launch_q8r_cfg(const SplitParams& p, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tks,
+                                  const CUtensorMap& tvs, int grid, cudaStream_t stream) {
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e =
+      set_smem_limit_once(split_decode_q8r_kernel<Cfg>, Cfg::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(split_decode_q8r_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes,
+                          stream, tk, tv, tks, tvs, p);
+}
+
 cudaError_t launch_split_q8(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tks, const CUtensorMap& tvs, int d, int kind,
                             int grid, cudaStream_t stream) {
   if (d == 128)
-    return kind == 1 ? launch_q8_cfg<Q8D128<1>>(p, tk, tv, tks, tvs, grid, stream)
-                     : launch_q8_cfg<Q8D128<2>>(p, tk, tv, tks, tvs, grid, stream);
+    return kind == 1 ? launch_q8r_cfg<Q8D128<1>>(p, tk, tv, tks, tvs, grid, stream)
+                     : launch_q8r_cfg<Q8D128<2>>(p, tk, tv, tks, tvs, grid, stream);
   return kind == 1 ? launch_q8_cfg<Q8D64<1>>(p, tk, tv, tks, tvs, grid, stream)
                    : launch_q8_cfg<Q8D64<2>>(p, tk, tv, tks, tvs, grid, stream);
 }

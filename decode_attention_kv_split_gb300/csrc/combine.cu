@@ -18,18 +18,20 @@
 
 namespace da {
 
-// One CTA of 16 warps per (b, query head).  Warp w merges splits w, w+16,
-// ... in one pass, 16 in flight, keeping a running maximum of the lse
-// values it has seen (the online form of the combine; every weight is taken
-// against the same maximum that scales the warp's sum).  Each lane holds D/32
-// consecutive columns.  The 16 warp results meet in shared memory and are
-// merged the same way.
-constexpr int kCombineWarps = 16;
-// Dynamic shared memory of one combine CTA.  Only the first
-// kCombineWarps * (D + 2) floats are used; the request is sized so that at
-// most two CTAs share an SM.  The grid may launch while the split kernel
-// drains, and without the cap its CTAs pile up on the first SMs to free up.
-constexpr int kCombineSmemBytes = 96 * 1024;
+// One CTA of W warps per (b, query head).  Warp w merges splits w, w+W, ...
+// in one pass, NB in flight, keeping a running maximum of the lse values it
+// has seen (the online form of the combine; every weight is taken against the
+// same maximum that scales the warp's sum).  Each lane holds D/32 consecutive
+// columns.  The W warp results meet in shared memory and are merged the same
+// way.  W = 16 when a head may have more than 8 * 17 splits (long contexts
+// with hundreds of splits), else W = 8 (and always for balanced pieces), so
+// that four CTAs fit on an SM and a batch of many heads merges in one wave.
+// Dynamic shared memory of one combine CTA: only W * (D + 2) floats are used;
+// the request caps the CTAs per SM (two of 16 warps, four of 8).  The grid
+// may launch while the split kernel drains, and without the cap its CTAs pile
+// up on the first SMs to free up.
+template <int W>
+constexpr int combine_smem_bytes() { return W == 16 ? 96 * 1024 : 48 * 1024; }
 
 // EPL consecutive floats (EPL * 4-byte aligned) through L2, as vector loads.
 template <int EPL>
@@ -46,11 +48,11 @@ __device__ __forceinline__ void ldcg_vec(float (&v)[EPL], const float* src) {
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32, 2)
+template <int D, int W>
+__global__ void __launch_bounds__(W * 32, 32 / W)
     lse_combine_kernel(const SplitParams p, int heads_per_cta) {
   constexpr int EPL = D / 32;
-  constexpr int kWarps = kCombineWarps;
+  constexpr int kWarps = W;
   extern __shared__ float csm[];
   float* red_acc = csm;                 // [kWarps][D]
   float* red_m = csm + kWarps * D;      // [kWarps]
@@ -150,14 +152,26 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
   }
 }
 
+template <int D, int W>
+static cudaError_t launch_combine_dw(const SplitParams& p, int heads_per_cta,
+                                     cudaStream_t stream) {
+  constexpr int kSmem = combine_smem_bytes<W>();
+  static_assert(W * (D + 2) * 4 <= kSmem, "combine scratch");
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(lse_combine_kernel<D, W>, kSmem, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(lse_combine_kernel<D, W>, p.B * p.h_q, W * 32, size_t(kSmem), stream,
+                          p, heads_per_cta);
+}
+
 template <int D>
 static cudaError_t launch_combine_d(const SplitParams& p, int heads_per_cta, cudaStream_t stream) {
-  static_assert(kCombineWarps * (D + 2) * 4 <= kCombineSmemBytes, "combine scratch");
-  static std::atomic<unsigned long long> smem_set{0};
-  const cudaError_t e = set_smem_limit_once(lse_combine_kernel<D>, kCombineSmemBytes, smem_set);
-  if (e != cudaSuccess) return e;
-  return launch_dependent(lse_combine_kernel<D>, p.B * p.h_q, kCombineWarps * 32,
-                          size_t(kCombineSmemBytes), stream, p, heads_per_cta);
+  constexpr int NB8 = D == 128 ? 17 : (D == 64 ? 16 : 8);  // splits in flight per warp
+  // balanced pieces: max_splits is one slot per CTA, but a unit rarely spans
+  // more than a few pieces (8 warps take any count, in more than one pass)
+  if (p.max_splits > 8 * NB8 && !p.balanced)
+    return launch_combine_dw<D, 16>(p, heads_per_cta, stream);
+  return launch_combine_dw<D, 8>(p, heads_per_cta, stream);
 }
 
 cudaError_t launch_combine(const SplitParams& p, int d, int heads_per_cta, cudaStream_t stream) {

@@ -720,58 +720,72 @@ __device__ __forceinline__ void store_out(const SplitParams& p, size_t idx, floa
 }
 
 // ---------------------------------------------------------------------------
-// End of a work item, shared by every split kernel.
+// End of a work item, shared by the split kernels with consumer warps.
 //
 // The consumer warps have written, per (key warp, head), their running max m
 // (log2 domain), running sum l and unnormalised accumulator into shared
 // slots.  This merges the KW key warps of each head group by log-sum-exp and
 // writes the item's normalised output: straight to `out` when the sequence
 // has a single split, else to its partial slot with its log-sum-exp for the
-// combine kernel.  All consumer threads call it together.
+// combine kernel.  All `nthreads` consumer threads call it together (it
+// synchronises them on named barrier 1).
+//   Phase A: one thread per head takes the maximum over the KW warps, the
+//            weight f_k = 2^(m_k - M) of each warp and the denominator
+//            L = sum_k f_k l_k, and leaves f_k in place of m_k and 1 / L in
+//            place of the head's first l (no other thread reads them).
+//   Phase B: all threads, one output element (head, column) at a time:
+//            out = (sum_k f_k acc_k) / L, consecutive threads on consecutive
+//            columns.
 // ---------------------------------------------------------------------------
 template <int D, int HG, int KW, int HPW, int SLOT_STRIDE>
 __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it,
-                                            const float* epi_acc, const float* epi_m,
-                                            const float* epi_l, int ctid, int nthreads,
-                                            volatile int* abort_flag) {
+                                            const float* epi_acc, float* epi_m, float* epi_l,
+                                            int ctid, int nthreads, volatile int* abort_flag) {
   constexpr int GC = HG * HPW;  // query heads of this item
-  if (*abort_flag) return;
+  static_assert(KW >= 2, "phase A keeps 1 / L in the second l slot");
   const int head0 = it.hc * GC;  // group-local index of the item's first head
   const int nh = min(GC, p.group - head0);
   const size_t bh0 = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + head0;
   const bool single = it.nv == 1;
+  if (ctid < GC) {
+    const int h = ctid, hg = h / HPW, hw = h - hg * HPW;
+    float m[KW], M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < KW; ++k) {
+      m[k] = epi_m[(hg * KW + k) * HPW + hw];
+      M = fmaxf(M, m[k]);
+    }
+    const float M_use = M == -INFINITY ? 0.f : M;  // an empty item: every l is 0
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < KW; ++k) {
+      const float f = ex2(m[k] - M_use);
+      L += f * epi_l[(hg * KW + k) * HPW + hw];
+      epi_m[(hg * KW + k) * HPW + hw] = f;
+    }
+    epi_l[(hg * KW + 1) * HPW + hw] = L > 0.f ? __fdividef(1.f, L) : 0.f;
+    if (h < nh && !*abort_flag) {
+      const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
+      if (!single) p.lse_part[(bh0 + h) * p.max_splits + it.split] = lse2;
+      else if (p.lse_out) p.lse_out[bh0 + h] = lse2 * kLn2;
+    }
+  }
+  named_bar_sync(1, nthreads);
   const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
   const size_t base = single ? bh0 * D : (bh0 * p.max_splits + it.split) * D;
-  for (int d = ctid; d < D; d += nthreads) {
-    // the heads are independent: unrolled, their loads and merges overlap
+  for (int idx = ctid; idx < nh * D; idx += nthreads) {
+    const int h = idx / D, d = idx - h * D;
+    const int hg = h / HPW, hw = h - hg * HPW;
+    float sum = 0.f;
 #pragma unroll
-    for (int h = 0; h < GC; ++h) {
-      const int hg = h / HPW, hw = h - hg * HPW;
-      float m[KW], M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < KW; ++k) {
-        m[k] = epi_m[(hg * KW + k) * HPW + hw];
-        M = fmaxf(M, m[k]);
-      }
-      const float M_use = M == -INFINITY ? 0.f : M;  // an empty item: every l is 0
-      float L = 0.f, sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < KW; ++k) {
-        const int sid = hg * KW + k;
-        const float f = ex2(m[k] - M_use);
-        L += f * epi_l[sid * HPW + hw];
-        sum += f * epi_acc[(sid * HPW + hw) * SLOT_STRIDE + d];
-      }
-      if (h < nh) {
-        const float val = L > 0.f ? __fdividef(sum, L) : 0.f;
-        if (single) store_out(p, base + h * stride + d, val);
-        else p.o_part[base + h * stride + d] = val;
-        if (d == 0) {
-          const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
-          if (!single) p.lse_part[(bh0 + h) * p.max_splits + it.split] = lse2;
-          else if (p.lse_out) p.lse_out[bh0 + h] = lse2 * kLn2;
-        }
-      }
+    for (int k = 0; k < KW; ++k) {
+      const int sid = hg * KW + k;
+      sum += epi_m[sid * HPW + hw] * epi_acc[(sid * HPW + hw) * SLOT_STRIDE + d];
+    }
+    const float val = sum * epi_l[(hg * KW + 1) * HPW + hw];
+    if (!*abort_flag) {
+      if (single) store_out(p, base + h * stride + d, val);
+      else p.o_part[base + h * stride + d] = val;
     }
   }
 }

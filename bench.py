@@ -52,24 +52,37 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_family(w) -> str:
+    """Source file of the split kernel a workload runs."""
+    if W.is_q8(w):
+        return "decode_q8.cu"
+    if w.dtype == torch.float32:
+        return "decode_fp32.cu"
+    if w.d_k == 128 and w.d_v == 128 and w.h_q // w.h_kv > 8:
+        return "decode_tc5.cu"
+    return "decode_bf16.cu"
+
+
+def kernel_source_hash(w) -> str:
+    """Hash of the sources that decide a workload's decode launches: the split
+    kernel's file, the shared device code, the combine and the host planner."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_kv_split_gb300", "csrc")
-    for fn in ("common.cuh", "decode_bf16.cu", "decode_fp32.cu", "decode_tc5.cu"):  # split kernels
+    for fn in ("common.cuh", "combine.cu", "api.cu", kernel_family(w)):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(w):
     """DRAM bytes per decode launch from a committed ncu capture, if it was taken
     on the current kernel sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        e = d.get(w.name)
+        if e and e.get("kernel_source_hash") == kernel_source_hash(w):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -543,7 +556,7 @@ def run_ours(args, w, world, rank, local):
     step_bytes = h.step_bytes()
     peak, peak_kind = peaks()
     achieved = step_bytes / (ms_per_step / 1e3) / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w)
     bytes_str = f"{step_bytes / 1e6:.1f} MB per step"
     if h.n_rot * h.kv_touch < 4 * L2_BYTES:
         bytes_str += " (L2-resident)"

@@ -390,29 +390,34 @@ __device__ __forceinline__ int bal_len(const Schedule& s, int b) {
   return n > 0 ? n : 1;
 }
 
+// Stream positions fit in 32 bits: the host only takes this list when the
+// rows of a launch slice number fewer than 2^31, and a boundary c * piece is
+// below R + piece < 2^32.
+
 // The unit holding stream position x (0 <= x < R) and the position where it starts.
-__device__ __forceinline__ int bal_unit(const SplitParams& p, const Schedule& s, long long x,
-                                        long long& start) {
-  const long long per_seq = p.h_kv * p.head_chunks;
+__device__ __forceinline__ int bal_unit(const SplitParams& p, const Schedule& s, uint32_t x,
+                                        uint32_t& start) {
+  const uint32_t per_seq = uint32_t(p.h_kv * p.head_chunks);
   int lo = 0, hi = p.B - 1;  // last b with per_seq * first[b] <= x
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (per_seq * s.first(mid) <= x) lo = mid; else hi = mid - 1;
+    if (per_seq * uint32_t(s.first(mid)) <= x) lo = mid; else hi = mid - 1;
   }
-  const long long len = bal_len(s, lo);
-  const long long j = (x - per_seq * s.first(lo)) / len;
-  start = per_seq * s.first(lo) + j * len;
-  return int(lo * per_seq + j);
+  const uint32_t len = uint32_t(bal_len(s, lo));
+  const uint32_t base = per_seq * uint32_t(s.first(lo));
+  const uint32_t j = (x - base) / len;
+  start = base + j * len;
+  return int(uint32_t(lo) * per_seq + j);
 }
 
 // Stream position of boundary c (0 .. gridDim.x).
 template <int TILE>
-__device__ __forceinline__ long long bal_cut(const SplitParams& p, const Schedule& s, int c) {
-  const long long R = (long long)(p.h_kv * p.head_chunks) * s.first(p.B);
-  const long long x = (long long)c * s.piece;
+__device__ __forceinline__ uint32_t bal_cut(const SplitParams& p, const Schedule& s, int c) {
+  const uint32_t R = uint32_t(p.h_kv * p.head_chunks) * uint32_t(s.first(p.B));
+  const uint32_t x = uint32_t(c) * uint32_t(s.piece);
   if (c <= 0) return 0;
   if (x >= R) return R;
-  long long start;
+  uint32_t start;
   bal_unit(p, s, x, start);
   return start + (x - start) / TILE * TILE;
 }
@@ -422,13 +427,14 @@ template <int TILE>
 __device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, int c, int u) {
   const int per_seq = p.h_kv * p.head_chunks;
   const int b = u / per_seq, j = u - (u / per_seq) * per_seq;
-  const long long len = bal_len(s, b);
-  const long long U = (long long)per_seq * s.first(b) + j * len;
-  const long long lo = bal_cut<TILE>(p, s, c), hi = bal_cut<TILE>(p, s, c + 1);
+  const uint32_t len = uint32_t(bal_len(s, b));
+  const uint32_t piece = uint32_t(s.piece);
+  const uint32_t U = uint32_t(per_seq) * uint32_t(s.first(b)) + uint32_t(j) * len;
+  const uint32_t lo = bal_cut<TILE>(p, s, c), hi = bal_cut<TILE>(p, s, c + 1);
   // first CTA whose piece reaches past U; last CTA whose piece starts before U + len
-  int c0 = int(U / s.piece);
+  int c0 = int(U / piece);
   while (c0 + 1 < int(gridDim.x) && bal_cut<TILE>(p, s, c0 + 1) <= U) ++c0;
-  int c1 = int((U + len - 1) / s.piece);
+  int c1 = int((U + len - 1) / piece);
   if (c1 > int(gridDim.x) - 1) c1 = int(gridDim.x) - 1;
   Item it;
   it.b = b;
@@ -437,11 +443,11 @@ __device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, i
   it.split = c - c0;
   it.nv = c1 - c0 + 1;
   const int n = len_of(s.lens(b));
-  const long long beg = (lo > U ? lo : U) - U;
-  long long end = (hi < U + len ? hi : U + len) - U;
+  const int beg = int((lo > U ? lo : U) - U);
+  int end = int((hi < U + len ? hi : U + len) - U);
   if (end > n) end = n;  // an empty sequence's one stream row holds no data
-  it.row_begin = int(beg < end ? beg : end);
-  it.row_end = int(end);
+  it.row_begin = beg < end ? beg : end;
+  it.row_end = end;
   const int last = (s.lens(b) & kAppendFlag) ? n - 1 : -1;
   it.new_row = (last >= it.row_begin && last < it.row_end) ? last : -1;
   it.tiles = (it.row_end - it.row_begin + TILE - 1) / TILE;
@@ -484,26 +490,29 @@ __device__ __forceinline__ Item cta_item(const SplitParams& p, const Schedule& s
 // are summed over the sequences by all warps of the CTA; every reduction runs
 // in a fixed order, so every CTA picks the same length.  All threads call this
 // with the CTA-wide row total and longest length.
-__device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* lens, int tile,
-                                            int grid, float rows, int nmax,
+template <int TILE>
+__device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* lens, int grid,
+                                            float rows, int nmax,
                                             int* red /* shared, kSchedRedWords */) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int longest = nmax > 0 ? nmax : 1;
   const int per_seq = p.h_kv * p.head_chunks;
   const int units = p.B * per_seq;
   const int k = lane;
-  long long c;
+  uint32_t c;  // candidate length, at most 2^30 (32-bit arithmetic throughout)
   if (k < 16) {
-    c = (long long)p.chunk_min << k;
+    const unsigned long long c64 = (unsigned long long)p.chunk_min << k;
+    c = c64 > (1ull << 30) ? (1u << 30) : uint32_t(c64);
   } else {
     int pieces = (k - 15) * grid / units;
     if (pieces < 1) pieces = 1;
-    c = longest / pieces + (longest % pieces != 0);
+    c = uint32_t(longest / pieces + (longest % pieces != 0));
   }
-  c = (c + tile - 1) / tile * tile;
-  if (c < p.chunk_min) c = p.chunk_min;
-  if (c > (1 << 30)) c = 1 << 30;
+  c = (c + TILE - 1) / TILE * TILE;
+  if (c < uint32_t(p.chunk_min)) c = uint32_t(p.chunk_min);
+  if (c > (1u << 30)) c = 1u << 30;
   const int ci = int(c);
+  const int tile = TILE;
   // power-of-two candidates stop after the first one covering everything
   const bool candidate = k >= 16 || k == 0 || ((long long)p.chunk_min << (k - 1)) < longest;
   int items = 0;
@@ -617,14 +626,14 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
     }
     __syncthreads();
     s.balanced = 1;
-    const long long R = (long long)per_seq * first[p.B];
-    long long piece = (R + gridDim.x - 1) / gridDim.x;
+    const uint32_t R = uint32_t(per_seq) * uint32_t(first[p.B]);
+    uint32_t piece = (R + gridDim.x - 1) / gridDim.x;
     if (piece < TILE) piece = TILE;  // so that no two boundaries round to the same row
     s.piece = int(piece);
-    const long long lo = bal_cut<TILE>(p, s, int(blockIdx.x));
-    const long long hi = bal_cut<TILE>(p, s, int(blockIdx.x) + 1);
+    const uint32_t lo = bal_cut<TILE>(p, s, int(blockIdx.x));
+    const uint32_t hi = bal_cut<TILE>(p, s, int(blockIdx.x) + 1);
     if (lo < hi) {
-      long long start;
+      uint32_t start;
       s.u0 = bal_unit(p, s, lo, start);
       s.mine = bal_unit(p, s, hi - 1, start) - s.u0 + 1;
     }
@@ -668,7 +677,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
       all_rows += __int_as_float(red[16 * 32 + w]);
       all_max = max(all_max, red[16 * 32 + 32 + w]);
     }
-    s.chunk = choose_chunk(p, lens, TILE, gridDim.x, all_rows, all_max, red);
+    s.chunk = choose_chunk<TILE>(p, lens, gridDim.x, all_rows, all_max, red);
   }
   // exclusive scan of the full-split items per sequence by warp 0
   if (tid < 32) {

@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       if (lane == 0) mbar_arrive(p_full0 + 8 * (j & 1));
     }
     // ---- item epilogue
-    if (it.tiles > 0) wait_pv(j - 1);
+    // The softmax sums are final: reduce them while the last P.V completes.
     float* gred = gred_of(j & 1);
     // per-head sums over the 128 rows
 #pragma unroll
@@ -653,6 +653,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       L[h] = gred[h] + gred[HT + h] + gred[2 * HT + h] + gred[3 * HT + h];
       inv_l[h] = L[h] > 0.f ? __fdividef(1.f, L[h]) : 0.f;
     }
+    if (it.tiles > 0) wait_pv(j - 1);  // O is complete in TMEM
     float o[HT];
     const bool epi_live = __all_sync(0xffffffffu, !*abort_flag);  // warp-uniform, as above
     if (it.tiles > 0 && epi_live) {

@@ -601,7 +601,7 @@ def run_ours(args, w, world, rank, local):
 
 
 SWEEP_CONTEXTS = (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
-SWEEP_SHAPES = ("gqa_llama3_8b", "mqa_g32", "long_llama2_70b", "mha_fp32")
+SWEEP_SHAPES = ("gqa_llama3_8b", "mqa_g32", "long_llama2_70b", "mha_fp32", "long_llama2_70b_fp8")
 
 
 def run_sweep(args):

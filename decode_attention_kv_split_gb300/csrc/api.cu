@@ -309,18 +309,20 @@ int make_plan(int B, int h_q, int h_kv, int d, int d_v, int n_max, int dtype_arg
 // Workspace of one launch: a header word (the split length the kernels
 // used), partial outputs, partial log-sum-exps.
 struct WorkspaceLayout {
-  size_t header, o_part, lse_part, total;
+  size_t header, o_part, lse_part, hints, total;
 };
 
 WorkspaceLayout workspace_layout(const Plan& pl, int h_q, int d) {
-  WorkspaceLayout w{0, 0, 0, 0};
+  WorkspaceLayout w{0, 0, 0, 0, 0};
   if (pl.max_splits <= 1) return w;
   const size_t heads = size_t(pl.batch_per_launch) * h_q;
   w.header = 0;
   // header word; in balanced mode the per-unit partial counts follow it
   w.o_part = pl.balanced ? 256 + (size_t(pl.units) * 4 + 255) / 256 * 256 : 256;
   w.lse_part = w.o_part + heads * pl.max_splits * d * sizeof(float);
-  w.total = w.lse_part + heads * pl.max_splits * sizeof(float);
+  // then each CTA's first-tile hint for the next call (16 bytes per CTA)
+  w.hints = (w.lse_part + heads * pl.max_splits * sizeof(float) + 255) / 256 * 256;
+  w.total = w.hints + size_t(da::kMaxHintCtas) * 16;
   return w;
 }
 
@@ -402,6 +404,7 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.chunk_out = wl.total ? reinterpret_cast<int*>(ws + wl.header) : nullptr;
     p.balanced = pl.balanced ? 1 : 0;
     p.unit_nv = pl.balanced ? reinterpret_cast<int*>(ws + 256) : nullptr;
+    p.hints = wl.total ? reinterpret_cast<int4*>(ws + wl.hints) : nullptr;
     p.dev_error = dev_error;
     p.append = k_new != nullptr;
     p.k_new = k_new ? static_cast<const char*>(k_new) + size_t(b0) * h_kv * d_k * es : nullptr;

@@ -58,6 +58,7 @@ struct SplitParams {
   int chunk_fixed;               // > 0: rows per split chosen by the caller
   int balanced;                  // 1: cut all units' rows into one equal piece per CTA
   int* unit_nv;                  // balanced: [units] partial count of each unit (workspace)
+  int4* hints;                   // nullable: [gridDim.x] first tiles of each CTA (workspace)
   int chunk_min;                 // else: smallest rows per split the device may choose
   int max_splits;                // partial slots per query head (ceil(n_max / chunk))
   float cta_speed;               // one CTA's streaming rate / its even share (split-length model)
@@ -796,6 +797,77 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
       if (single) store_out(p, base + h * stride + d, val);
       else p.o_part[base + h * stride + d] = val;
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// First-tile hints.  A decode call usually follows one of the same shape on
+// the same workspace (the previous decode step), and a CTA's first tiles are
+// then the same rows as last time.  Each CTA leaves the coordinates of its
+// first tiles in the workspace; at the next launch its producer reads them
+// and asks for those tiles to be brought into L2 before it waits for the
+// previous grid and builds its work list (~1.5-4 us in which HBM would
+// otherwise idle).  An L2 prefetch is only a hint: L2 stays coherent with
+// any later write, so a stale or wrong guess costs bandwidth, never a result.
+// Hint words: {z, y0, tiles, check} with check = z ^ y0 ^ tiles ^ kHintSeal.
+// ---------------------------------------------------------------------------
+constexpr int kHintSeal = 0x5a17c0de;
+constexpr int kMaxHintCtas = 1024;
+
+// L2 prefetch of one box of a 3-D tiled tensor map.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// L2 prefetch of one box of a 2-D tiled tensor map.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// This CTA's hint from the previous launch, if it is well formed and inside
+// this launch's tensors: rows [y0, y0 + tiles * TILE) of kv head z.  Called
+// before griddepcontrol.wait: the words may be stale, never unsafe to use.
+template <int TILE>
+__device__ __forceinline__ bool read_hint(const SplitParams& p, int max_tiles, int& z, int& y0,
+                                          int& tiles) {
+  if (!p.hints || blockIdx.x >= unsigned(kMaxHintCtas)) return false;
+  const int4 h = __ldcg(p.hints + blockIdx.x);
+  z = h.x, y0 = h.y, tiles = h.z;
+  if ((h.x ^ h.y ^ h.z ^ kHintSeal) != h.w) return false;
+  const int z0 = p.b_offset * p.h_kv, z1 = (p.b_offset + p.B) * p.h_kv;
+  if (z < z0 || z >= z1 || y0 < 0 || y0 >= p.n_max || tiles < 1) return false;
+  if (tiles > max_tiles) tiles = max_tiles;
+  return true;
+}
+
+// After the work list is built: record this CTA's first tiles for the next launch.
+template <int TILE>
+__device__ __forceinline__ void write_hint(const SplitParams& p, const Item& it, int max_tiles) {
+  if (!p.hints || blockIdx.x >= unsigned(kMaxHintCtas)) return;
+  const int z = (p.b_offset + it.b) * p.h_kv + it.kvh;
+  const int y0 = it.row_begin;
+  const int tiles = it.tiles < max_tiles ? it.tiles : max_tiles;
+  p.hints[blockIdx.x] = make_int4(z, y0, tiles, z ^ y0 ^ tiles ^ kHintSeal);
+}
+
+// Producer lane, before waiting for the previous grid: L2 prefetch of the
+// hinted tiles of K (NBOX_K boxes of BOX_COLS columns per tile) and V.
+template <int TILE, int NBOX_K, int NBOX_V, int BOX_COLS>
+__device__ __forceinline__ void prefetch_hinted(const SplitParams& p, const CUtensorMap* tmK,
+                                                const CUtensorMap* tmV, int max_tiles) {
+  int z, y0, tiles;
+  if (!read_hint<TILE>(p, max_tiles, z, y0, tiles)) return;
+  for (int t = 0; t < tiles && y0 + t * TILE < p.n_max; ++t) {
+#pragma unroll
+    for (int h = 0; h < NBOX_K; ++h) tma_prefetch_3d(tmK, h * BOX_COLS, y0 + t * TILE, z);
+#pragma unroll
+    for (int h = 0; h < NBOX_V; ++h) tma_prefetch_3d(tmV, h * BOX_COLS, y0 + t * TILE, z);
   }
 }
 

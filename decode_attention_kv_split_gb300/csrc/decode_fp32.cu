@@ -94,12 +94,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
+  if (threadIdx.x == Cfg::kConsumerThreads)  // producer lane: L2 prefetch of the hinted tiles
+    prefetch_hinted<Cfg::kTile, 1, 1, 0>(p, &tmK, &tmV, STAGES);
   // Launched as a programmatic dependent: the set-up above overlaps the tail
   // of the previous grid on the stream, which may have produced seq_lens, q,
-  // the caches or the new rows.  Nothing before this line reads them.
+  // the caches or the new rows.  Nothing before this line reads them (the
+  // hinted prefetch only warms L2).
   wait_for_prerequisite_grid();
   const Schedule sched = build_schedule<Cfg::kTile>(p, sched_words);
   allow_dependent_launch();
+  if (threadIdx.x == 0 && sched.mine > 0) write_hint<Cfg::kTile>(p, cta_item<Cfg::kTile>(p, sched, 0), STAGES);
 
   // ------------------------------------------------------------------ producer
   if (warp == W) {

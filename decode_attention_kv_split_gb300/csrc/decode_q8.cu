@@ -94,6 +94,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 }  // namespace q8
 
+// Producer lane, before waiting for the previous grid: L2 prefetch of the
+// hinted tiles of the codes (one box per tile) and of their row scales.
+template <int TILE>
+__device__ __forceinline__ void prefetch_hinted_q8(const SplitParams& p, const CUtensorMap* tmK,
+                                                   const CUtensorMap* tmV, const CUtensorMap* tmKs,
+                                                   const CUtensorMap* tmVs, int max_tiles) {
+  int z, y0, tiles;
+  if (!read_hint<TILE>(p, max_tiles, z, y0, tiles)) return;
+  if ((y0 & 3) != 0) return;  // the row-scale maps take x = row: 16-byte aligned starts only
+  for (int t = 0; t < tiles && y0 + t * TILE < p.n_max; ++t) {
+    tma_prefetch_3d(tmK, 0, y0 + t * TILE, z);
+    tma_prefetch_3d(tmV, 0, y0 + t * TILE, z);
+    tma_prefetch_2d(tmKs, y0 + t * TILE, z);
+    tma_prefetch_2d(tmVs, y0 + t * TILE, z);
+  }
+}
+
 template <int D_, int KW_, int KBW_, int STAGES_, int KIND_>
 struct Q8Cfg {
   static constexpr int D = D_;            // head dim (d_k == d_v)
@@ -256,11 +273,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_tmap(&tmKs);
     prefetch_tmap(&tmVs);
   }
+  if (threadIdx.x == Cfg::kConsumerThreads)  // producer lane: L2 prefetch of the hinted tiles
+    prefetch_hinted_q8<T>(p, &tmK, &tmV, &tmKs, &tmVs, STAGES);
   // Launched as a programmatic dependent: nothing before this line reads
-  // memory that the previous grid on the stream may write.
+  // memory that the previous grid on the stream may write (the hinted
+  // prefetch only warms L2).
   wait_for_prerequisite_grid();
   const Schedule sched = build_schedule<T>(p, sched_words);
   allow_dependent_launch();
+  if (threadIdx.x == 0 && sched.mine > 0) write_hint<T>(p, cta_item<T>(p, sched, 0), STAGES);
 
   // ------------------------------------------------------------------ producer
   if (warp == KW) {
@@ -643,11 +664,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_tmap(&tmKs);
     prefetch_tmap(&tmVs);
   }
+  if (threadIdx.x == Cfg::kConsumerThreads)  // producer lane: L2 prefetch of the hinted tiles
+    prefetch_hinted_q8<T>(p, &tmK, &tmV, &tmKs, &tmVs, STAGES);
   // Launched as a programmatic dependent: nothing before this line reads
-  // memory that the previous grid on the stream may write.
+  // memory that the previous grid on the stream may write (the hinted
+  // prefetch only warms L2).
   wait_for_prerequisite_grid();
   const Schedule sched = build_schedule<T>(p, sched_words);
   allow_dependent_launch();
+  if (threadIdx.x == 0 && sched.mine > 0) write_hint<T>(p, cta_item<T>(p, sched, 0), STAGES);
 
   // ------------------------------------------------------------------ producer
   if (warp == KW) {

@@ -298,14 +298,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
+  if (threadIdx.x == 8 * 32)  // producer warp: L2 prefetch of the hinted tiles
+    prefetch_hinted<T, 2, 2, 64>(p, &tmK, &tmV, KST);
   // Launched as a programmatic dependent: the set-up above overlaps the tail
   // of the previous grid on the stream, which may have produced seq_lens, q,
-  // the caches or the new rows.  Nothing before this line reads them.
+  // the caches or the new rows.  Nothing before this line reads them (the
+  // hinted prefetch only warms L2).
   wait_for_prerequisite_grid();
   tc5::fence_before();
   const Schedule sched = build_schedule<T>(p, sched_words);
   tc5::fence_after();
   allow_dependent_launch();
+  if (threadIdx.x == 0 && sched.mine > 0) write_hint<T>(p, cta_item<T>(p, sched, 0), KST);
   const uint32_t tmem = *tmem_slot;
   const uint32_t s_col0 = tmem, o_col = tmem + 2 * NH;  // chain c at o_col + c * 2 NH
 

@@ -105,10 +105,12 @@ DA_API int decode_attn_resolve_splits(int B, int h_q, int h_kv, int d_k, int d_v
 
 /*
  * Bytes of device workspace decode_attn_ex needs for this request: a 256-byte
- * header and the per-split partial outputs and log-sum-exps (float32) of at
+ * header, the per-split partial outputs and log-sum-exps (float32) of at
  * most 512 sequences (larger batches run as several launches that reuse
- * it, one after the other on the stream).  0 when the request can only use
- * one split.  Returns 0 and sets *status (when non-NULL) to a
+ * it, one after the other on the stream) and 16 KB in which each CTA leaves
+ * the position of its first tiles for the next call on the same workspace
+ * (read back as an L2 prefetch hint: any content is safe).  0 when the
+ * request can only use one split.  Returns 0 and sets *status (when non-NULL) to a
  * negative da_status if the arguments are invalid.
  */
 DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int d_v, int n_max,

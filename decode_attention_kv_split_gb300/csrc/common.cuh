@@ -323,6 +323,7 @@ struct Schedule {
   int balanced;     // 1: items are the units one equal piece of the row stream touches
   int u0;           // balanced: the first unit of this CTA's piece
   int piece;        // balanced: rows per piece before tile alignment
+  const int* cuts;  // balanced: the gridDim.x + 1 boundaries, in shared memory
   __device__ __forceinline__ int first(int b) const { return w[b]; }
   __device__ __forceinline__ int lens(int b) const { return w[kSchedLens + b]; }
 };
@@ -431,10 +432,10 @@ __device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, i
   const uint32_t len = uint32_t(bal_len(s, b));
   const uint32_t piece = uint32_t(s.piece);
   const uint32_t U = uint32_t(per_seq) * uint32_t(s.first(b)) + uint32_t(j) * len;
-  const uint32_t lo = bal_cut<TILE>(p, s, c), hi = bal_cut<TILE>(p, s, c + 1);
+  const uint32_t lo = uint32_t(s.cuts[c]), hi = uint32_t(s.cuts[c + 1]);
   // first CTA whose piece reaches past U; last CTA whose piece starts before U + len
   int c0 = int(U / piece);
-  while (c0 + 1 < int(gridDim.x) && bal_cut<TILE>(p, s, c0 + 1) <= U) ++c0;
+  while (c0 + 1 < int(gridDim.x) && uint32_t(s.cuts[c0 + 1]) <= U) ++c0;
   int c1 = int((U + len - 1) / piece);
   if (c1 > int(gridDim.x) - 1) c1 = int(gridDim.x) - 1;
   Item it;
@@ -603,6 +604,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   s.balanced = 0;
   s.u0 = 0;
   s.piece = 0;
+  s.cuts = nullptr;
   s.chunk = 0;
   s.total = 0;
   s.mine = 0;
@@ -631,8 +633,13 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
     uint32_t piece = (R + gridDim.x - 1) / gridDim.x;
     if (piece < TILE) piece = TILE;  // so that no two boundaries round to the same row
     s.piece = int(piece);
-    const uint32_t lo = bal_cut<TILE>(p, s, int(blockIdx.x));
-    const uint32_t hi = bal_cut<TILE>(p, s, int(blockIdx.x) + 1);
+    // every boundary once, a thread each, into the reduction scratch
+    // (gridDim.x + 1 <= kSchedRedWords words; the host launches at most that many CTAs)
+    for (int c = tid; c <= int(gridDim.x); c += blockDim.x) red[c] = int(bal_cut<TILE>(p, s, c));
+    __syncthreads();
+    s.cuts = red;
+    const uint32_t lo = uint32_t(s.cuts[blockIdx.x]);
+    const uint32_t hi = uint32_t(s.cuts[blockIdx.x + 1]);
     if (lo < hi) {
       uint32_t start;
       s.u0 = bal_unit(p, s, lo, start);

@@ -400,3 +400,21 @@ def test_fused_append_sixteen_steps(o, dtype):
                                  scale, out.cpu(), TOL[dtype])
     torch.cuda.synchronize()
     assert np.array_equal(_bits(Kd.cpu()), Kw) and np.array_equal(_bits(Vd.cpu()), Vw)
+
+
+# ----------------------------------------------------------------- combine variants
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("splits", [40, 100, 200, 300])
+def test_combine_variants(o, dtype, splits):
+    """Split counts that select each merge layout: 8-warp CTAs (up to 136 splits,
+    one pass) and 16-warp CTAs (hundreds of splits, more than one pass at 300)."""
+    n_max = 300 * 128
+    lens = [n_max, n_max - 5000, 129]
+    q, K, V, lens_t, scale = make_case(3, 8, 2, 128, n_max, lens, dtype, seed=splits)
+    # the split length is a whole number of pipeline stages near n_max / splits;
+    # the counts still land in the layout each case is meant for
+    got = api.resolve_splits(3, 8, 2, 128, 128, n_max, dtype, splits)
+    lo, hi = {40: (2, 68), 100: (69, 136), 200: (137, 10**6), 300: (137, 10**6)}[splits]
+    assert lo <= got <= hi, got
+    out = gpu_decode(q, K, V, lens_t, num_splits=splits)
+    check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])

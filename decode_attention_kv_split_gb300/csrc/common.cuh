@@ -561,12 +561,37 @@ __device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* len
   return red[kSchedRedWords - 1];
 }
 
+// The rows a sequence contributes to the work list, from its seq_lens value:
+// clamped into [0, n_max], plus the appended row when there is room for it
+// (kAppendFlag set), else cut to the decoded row range.  `n_out` receives the
+// length after the append (the seq_lens_out value).
+__device__ __forceinline__ int list_len(const SplitParams& p, int n, bool& bad, bool& bad_pos,
+                                        int& n_out) {
+  bool app = false;
+  if (p.append) {
+    app = n >= 0 && n < p.n_max;  // room for the new row
+    bad_pos |= !app;
+  }
+  if (n < 0 || n > p.n_max) {
+    bad = true;
+    n = n < 0 ? 0 : p.n_max;
+  }
+  if (app) ++n;
+  n_out = n;
+  if (!app) {  // rows of the decoded range (all of them unless a range was asked for)
+    n = min(n, p.row_lim) - p.row_off;
+    n = n < 0 ? 0 : n;
+  }
+  return app ? (n | kAppendFlag) : n;
+}
+
 // Builds the work list in shared memory; every thread of the CTA must call it.
-// `sched` points at kSchedWords ints (16-byte aligned).  Reads seq_lens (and
-// writes seq_lens_out from CTA 0): call it after any wait for the grid that
-// produced them.
+// `sched` points at kSchedWords ints (16-byte aligned).  It writes nothing
+// but shared memory, so it may run before the wait for the previous grid,
+// on lengths that grid may still be writing: commit_schedule checks them
+// afterwards and builds again if any changed.
 template <int TILE>
-__device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sched) {
+__device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, int* sched) {
   int* first = sched;
   int* lens = sched + kSchedLens;
   int* red = sched + kSchedRed;
@@ -577,28 +602,14 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   float rows = 0.f;  // only feeds the split-length model; summed in a fixed order
   int nmax = 0;
   for (int b = tid; b < p.B; b += blockDim.x) {
-    int n = __ldg(p.seq_lens + b);
-    bool app = false;
-    if (p.append) {
-      app = n >= 0 && n < p.n_max;  // room for the new row
-      bad_pos |= !app;
-    }
-    if (n < 0 || n > p.n_max) {
-      bad = true;
-      n = n < 0 ? 0 : p.n_max;
-    }
-    if (app) ++n;
-    if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n;
-    if (!app) {  // rows of the decoded range (all of them unless a range was asked for)
-      n = min(n, p.row_lim) - p.row_off;
-      n = n < 0 ? 0 : n;
-    }
-    lens[b] = app ? (n | kAppendFlag) : n;
+    int n_out;
+    const int lv = list_len(p, __ldcg(p.seq_lens + b), bad, bad_pos, n_out);  // through L2
+    const int n = len_of(lv);
+    lens[b] = lv;
     rows += float(n);
     nmax = n > nmax ? n : nmax;
   }
-  if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
-  if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
+  (void)bad, (void)bad_pos;
   Schedule s;
   s.w = sched;
   s.balanced = 0;
@@ -645,11 +656,9 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
       s.u0 = bal_unit(p, s, lo, start);
       s.mine = bal_unit(p, s, hi - 1, start) - s.u0 + 1;
     }
-    if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = -1;  // marks balanced
-    for (int t = tid; t < s.mine; t += blockDim.x) {
+    for (int t = tid; t < s.mine && t < kItemCache; t += blockDim.x) {
       const Item it = bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + t);
-      if (it.split == 0 && p.unit_nv) p.unit_nv[s.u0 + t] = it.nv;  // the unit's first CTA
-      if (t < kItemCache) {
+      {
         int* w = items + t * kItemWords;
         w[0] = it.b;
         w[1] = it.kvh;
@@ -710,7 +719,6 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   }
   __syncthreads();
   s.total = first[p.B] + per_seq * p.B;  // and one last split per unit
-  if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = s.chunk;
   // decode this CTA's first items, one per thread
   const int mine = s.total > int(blockIdx.x) ? (s.total - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
   s.mine = mine;
@@ -728,6 +736,42 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
   }
   __syncthreads();
   return s;
+}
+
+// After the wait for the previous grid: read seq_lens again (now final), build
+// the list again if any length differs from the one it was built on, then
+// make the list's global writes: seq_lens_out and the error bits (CTA 0), the
+// split length or balanced marker for the combine (CTA 0) and, in balanced
+// mode, each unit's partial count (its first CTA).  Every thread must call it.
+template <int TILE>
+__device__ __forceinline__ Schedule commit_schedule(const SplitParams& p, int* sched,
+                                                    Schedule s) {
+  const int* lens = sched + kSchedLens;
+  const int tid = threadIdx.x;
+  bool bad = false, bad_pos = false;
+  int changed = 0;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    int n_out;
+    const int lv = list_len(p, __ldcg(p.seq_lens + b), bad, bad_pos, n_out);
+    changed |= lv != lens[b];
+    if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n_out;
+  }
+  if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
+  if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
+  if (__syncthreads_or(changed)) s = build_schedule_core<TILE>(p, sched);
+  if (blockIdx.x == 0 && tid == 0 && p.chunk_out) *p.chunk_out = s.balanced ? -1 : s.chunk;
+  if (s.balanced && p.unit_nv)
+    for (int t = tid; t < s.mine; t += blockDim.x) {
+      const Item it = bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + t);
+      if (it.split == 0) p.unit_nv[s.u0 + t] = it.nv;  // the unit's first CTA
+    }
+  return s;
+}
+
+// The whole work list when nothing can change under it (a single call).
+template <int TILE>
+__device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sched) {
+  return commit_schedule<TILE>(p, sched, build_schedule_core<TILE>(p, sched));
 }
 
 // One element of the final output, rounded to bf16 when the caller asked for it.

@@ -116,10 +116,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_hinted<Cfg::kTile, Cfg::kHalvesK, Cfg::kHalvesV, 64>(p, &tmK, &tmV, STAGES);
   // Launched as a programmatic dependent: the set-up above overlaps the tail
   // of the previous grid on the stream, which may have produced seq_lens, q,
-  // the caches or the new rows.  Nothing before this line reads them (the
-  // hinted prefetch only warms L2).
+  // the caches or the new rows.  Before the wait below, only the hinted L2
+  // prefetch and the work list touch them: the prefetch is a hint, and the
+  // list is built on the lengths as they read now (shared memory only), then
+  // checked and built again if they changed once the wait is over.
+  Schedule sched = build_schedule_core<Cfg::kTile>(p, sched_words);
   wait_for_prerequisite_grid();
-  const Schedule sched = build_schedule<Cfg::kTile>(p, sched_words);
+  sched = commit_schedule<Cfg::kTile>(p, sched_words, sched);
   allow_dependent_launch();
   if (threadIdx.x == 0 && sched.mine > 0) write_hint<Cfg::kTile>(p, cta_item<Cfg::kTile>(p, sched, 0), STAGES);
 

@@ -275,11 +275,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
   if (threadIdx.x == Cfg::kConsumerThreads)  // producer lane: L2 prefetch of the hinted tiles
     prefetch_hinted_q8<T>(p, &tmK, &tmV, &tmKs, &tmVs, STAGES);
-  // Launched as a programmatic dependent: nothing before this line reads
-  // memory that the previous grid on the stream may write (the hinted
-  // prefetch only warms L2).
+  // Launched as a programmatic dependent: the set-up above overlaps the tail
+  // of the previous grid on the stream, which may have produced seq_lens, q,
+  // the caches or the new rows.  Before the wait below, only the hinted L2
+  // prefetch and the work list touch them: the prefetch is a hint, and the
+  // list is built on the lengths as they read now (shared memory only), then
+  // checked and built again if they changed once the wait is over.
+  Schedule sched = build_schedule_core<T>(p, sched_words);
   wait_for_prerequisite_grid();
-  const Schedule sched = build_schedule<T>(p, sched_words);
+  sched = commit_schedule<T>(p, sched_words, sched);
   allow_dependent_launch();
   if (threadIdx.x == 0 && sched.mine > 0) write_hint<T>(p, cta_item<T>(p, sched, 0), STAGES);
 
@@ -666,11 +670,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
   if (threadIdx.x == Cfg::kConsumerThreads)  // producer lane: L2 prefetch of the hinted tiles
     prefetch_hinted_q8<T>(p, &tmK, &tmV, &tmKs, &tmVs, STAGES);
-  // Launched as a programmatic dependent: nothing before this line reads
-  // memory that the previous grid on the stream may write (the hinted
-  // prefetch only warms L2).
+  // Launched as a programmatic dependent: the set-up above overlaps the tail
+  // of the previous grid on the stream, which may have produced seq_lens, q,
+  // the caches or the new rows.  Before the wait below, only the hinted L2
+  // prefetch and the work list touch them: the prefetch is a hint, and the
+  // list is built on the lengths as they read now (shared memory only), then
+  // checked and built again if they changed once the wait is over.
+  Schedule sched = build_schedule_core<T>(p, sched_words);
   wait_for_prerequisite_grid();
-  const Schedule sched = build_schedule<T>(p, sched_words);
+  sched = commit_schedule<T>(p, sched_words, sched);
   allow_dependent_launch();
   if (threadIdx.x == 0 && sched.mine > 0) write_hint<T>(p, cta_item<T>(p, sched, 0), STAGES);
 

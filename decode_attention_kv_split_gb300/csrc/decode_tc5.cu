@@ -302,11 +302,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_hinted<T, 2, 2, 64>(p, &tmK, &tmV, KST);
   // Launched as a programmatic dependent: the set-up above overlaps the tail
   // of the previous grid on the stream, which may have produced seq_lens, q,
-  // the caches or the new rows.  Nothing before this line reads them (the
-  // hinted prefetch only warms L2).
-  wait_for_prerequisite_grid();
+  // the caches or the new rows.  Before the wait below, only the hinted L2
+  // prefetch and the work list touch them: the prefetch is a hint, and the
+  // list is built on the lengths as they read now (shared memory only), then
+  // checked and built again if they changed once the wait is over.
   tc5::fence_before();
-  const Schedule sched = build_schedule<T>(p, sched_words);
+  Schedule sched = build_schedule_core<T>(p, sched_words);
+  wait_for_prerequisite_grid();
+  sched = commit_schedule<T>(p, sched_words, sched);
   tc5::fence_after();
   allow_dependent_launch();
   if (threadIdx.x == 0 && sched.mine > 0) write_hint<T>(p, cta_item<T>(p, sched, 0), KST);

@@ -26,6 +26,7 @@ DA_OUT_BF16 = 0x100  # dtype flag: out is bfloat16
 DEVERR_SEQ_LEN = 1
 DEVERR_POS = 2
 DEVERR_TIMEOUT = 4
+DEVERR_BOUNDS = 8    # set only by the bounds-checked test build
 
 _DTYPES = {torch.float32: DA_FP32, torch.bfloat16: DA_BF16}
 # 8-bit caches are passed as torch.int8 / torch.float8_e4m3fn tensors of codes

@@ -19,8 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdecode_attn.so")
 INCLUDE = os.path.join(ROOT, "include")
-# The same sources built with DA_TEST_HOOKS: short wait limits and a switch
-# that makes one producer withhold a stage.  Only the tests load it.
+# The same sources built with DA_TEST_HOOKS (short wait limits, a switch that
+# makes one producer withhold a stage) and DA_BOUNDS_CHECK (every global
+# index the kernels compute checked against its buffer; a bad one is skipped
+# and reported as DA_DEVERR_BOUNDS).  Only the tests load it.
 BUILD_TEST = os.path.join(PKG, "_build_test")
 LIB_TEST = os.path.join(PKG, "libdecode_attn_test.so")
 
@@ -59,7 +61,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, test_hooks: bool = Fa
         obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objects.append(obj)
         if ptxas_info or _stale(obj, [src, *headers]):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *(["-DDA_TEST_HOOKS"] if test_hooks else []), "-c",
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *(["-DDA_TEST_HOOKS", "-DDA_BOUNDS_CHECK"] if test_hooks else []), "-c",
                    src, "-o", obj]
             if ptxas_info:
                 cmd.insert(1, "-Xptxas=-v")

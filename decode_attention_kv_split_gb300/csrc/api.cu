@@ -405,6 +405,9 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.balanced = pl.balanced ? 1 : 0;
     p.unit_nv = pl.balanced ? reinterpret_cast<int*>(ws + 256) : nullptr;
     p.hints = wl.total ? reinterpret_cast<int4*>(ws + wl.hints) : nullptr;
+    p.out_elems = (long long)bn * h_q * d_v;
+    p.part_rows = wl.total ? (long long)bn * h_q * pl.max_splits : 0;
+    p.cache_rows = (long long)B * h_kv * n_max;
     p.dev_error = dev_error;
     p.append = k_new != nullptr;
     p.k_new = k_new ? static_cast<const char*>(k_new) + size_t(b0) * h_kv * d_k * es : nullptr;

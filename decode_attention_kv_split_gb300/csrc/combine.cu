@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(W * 32, 32 / W)
     nv = __ldcg(p.unit_nv + (b * p.h_kv + kvh) * p.head_chunks + hc);
   }
   if (nv <= 1) return;  // written by the split kernel
+  // (checked builds: the partial rows and the output row stay inside their buffers)
+  if (!DA_IN(p, size_t(bh) * p.max_splits + nv - 1, p.part_rows) ||
+      !DA_IN(p, size_t(bh) * D + D - 1, p.out_elems))
+    return;  // CTA-uniform
   const float* lse = p.lse_part + size_t(bh) * p.max_splits;
   const float* op = p.o_part + size_t(bh) * p.max_splits * D + lane * EPL;
 

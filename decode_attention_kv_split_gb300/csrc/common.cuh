@@ -59,6 +59,10 @@ struct SplitParams {
   int balanced;                  // 1: cut all units' rows into one equal piece per CTA
   int* unit_nv;                  // balanced: [units] partial count of each unit (workspace)
   int4* hints;                   // nullable: [gridDim.x] first tiles of each CTA (workspace)
+  // Extents for the checked build (set on every launch): elements of `out`
+  // in this slice, partial slots (B * h_q * max_splits), rows of K (and V) in
+  // the whole cache.
+  long long out_elems, part_rows, cache_rows;
   int chunk_min;                 // else: smallest rows per split the device may choose
   int max_splits;                // partial slots per query head (ceil(n_max / chunk))
   float cta_speed;               // one CTA's streaming rate / its even share (split-length model)
@@ -248,6 +252,22 @@ __device__ __forceinline__ bool lane_is_zero(int tid) { return (tid & 31) == 0; 
 __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
   if (dev_error) atomicOr(dev_error, bit);
 }
+
+// Checked builds (DA_BOUNDS_CHECK; the test build defines it): every index the
+// kernels compute from the caller's data for a global or shared-memory access
+// is checked against the extent of its buffer first; an index out of range
+// sets DA_DEVERR_BOUNDS and the access is skipped (never a trap).  Product
+// builds compile the checks away.
+#ifdef DA_BOUNDS_CHECK
+__device__ __forceinline__ bool in_range(int32_t* dev_error, long long i, long long n) {
+  if (i >= 0 && i < n) return true;
+  flag_error(dev_error, DA_DEVERR_BOUNDS);
+  return false;
+}
+#else
+__device__ __forceinline__ bool in_range(int32_t*, long long, long long) { return true; }
+#endif
+#define DA_IN(p, i, n) da::in_range((p).dev_error, (long long)(i), (long long)(n))
 
 // What a split-kernel variant needs from the host: its stage height (split
 // lengths are multiples of it), how many query heads one work item covers,
@@ -646,7 +666,8 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
     s.piece = int(piece);
     // every boundary once, a thread each, into the reduction scratch
     // (gridDim.x + 1 <= kSchedRedWords words; the host launches at most that many CTAs)
-    for (int c = tid; c <= int(gridDim.x); c += blockDim.x) red[c] = int(bal_cut<TILE>(p, s, c));
+    for (int c = tid; c <= int(gridDim.x); c += blockDim.x)
+      if (DA_IN(p, c, kSchedRedWords)) red[c] = int(bal_cut<TILE>(p, s, c));
     __syncthreads();
     s.cuts = red;
     const uint32_t lo = uint32_t(s.cuts[blockIdx.x]);
@@ -754,7 +775,7 @@ __device__ __forceinline__ Schedule commit_schedule(const SplitParams& p, int* s
     int n_out;
     const int lv = list_len(p, __ldcg(p.seq_lens + b), bad, bad_pos, n_out);
     changed |= lv != lens[b];
-    if (blockIdx.x == 0 && p.seq_lens_out) p.seq_lens_out[b] = n_out;
+    if (blockIdx.x == 0 && p.seq_lens_out && DA_IN(p, b, p.B)) p.seq_lens_out[b] = n_out;
   }
   if (bad && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_SEQ_LEN);
   if (bad_pos && blockIdx.x == 0) flag_error(p.dev_error, DA_DEVERR_POS);
@@ -763,7 +784,8 @@ __device__ __forceinline__ Schedule commit_schedule(const SplitParams& p, int* s
   if (s.balanced && p.unit_nv)
     for (int t = tid; t < s.mine; t += blockDim.x) {
       const Item it = bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + t);
-      if (it.split == 0) p.unit_nv[s.u0 + t] = it.nv;  // the unit's first CTA
+      if (it.split == 0 && DA_IN(p, s.u0 + t, p.B * p.h_kv * p.head_chunks))
+        p.unit_nv[s.u0 + t] = it.nv;  // the unit's first CTA
     }
   return s;
 }
@@ -776,6 +798,7 @@ __device__ __forceinline__ Schedule build_schedule(const SplitParams& p, int* sc
 
 // One element of the final output, rounded to bf16 when the caller asked for it.
 __device__ __forceinline__ void store_out(const SplitParams& p, size_t idx, float v) {
+  if (!DA_IN(p, idx, p.out_elems)) return;
   if (p.out_bf16) static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
   else static_cast<float*>(p.out)[idx] = v;
 }
@@ -827,8 +850,12 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
     epi_l[(hg * KW + 1) * HPW + hw] = L > 0.f ? __fdividef(1.f, L) : 0.f;
     if (h < nh && !*abort_flag) {
       const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
-      if (!single) p.lse_part[(bh0 + h) * p.max_splits + it.split] = lse2;
-      else if (p.lse_out) p.lse_out[bh0 + h] = lse2 * kLn2;
+      if (!single) {
+        if (DA_IN(p, (bh0 + h) * p.max_splits + it.split, p.part_rows))
+          p.lse_part[(bh0 + h) * p.max_splits + it.split] = lse2;
+      } else if (p.lse_out && DA_IN(p, bh0 + h, p.out_elems / D)) {
+        p.lse_out[bh0 + h] = lse2 * kLn2;
+      }
     }
   }
   named_bar_sync(1, nthreads);
@@ -846,7 +873,7 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
     const float val = sum * epi_l[(hg * KW + 1) * HPW + hw];
     if (!*abort_flag) {
       if (single) store_out(p, base + h * stride + d, val);
-      else p.o_part[base + h * stride + d] = val;
+      else if (DA_IN(p, base + h * stride + d, p.part_rows * D)) p.o_part[base + h * stride + d] = val;
     }
   }
 }
@@ -930,6 +957,7 @@ __device__ __forceinline__ void store_new_row(const SplitParams& p, const Item& 
                                               const uint8_t* slot, int lane) {
   const size_t head = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
   const size_t row = head * size_t(p.n_max) + size_t(it.new_row);
+  if (!DA_IN(p, row, p.cache_rows) || !DA_IN(p, it.new_row, p.n_max)) return;
   const uint4* ks = reinterpret_cast<const uint4*>(slot);
   const uint4* vs = reinterpret_cast<const uint4*>(slot + KROW);
   uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + row * KROW);
@@ -1032,23 +1060,22 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
       const uint32_t bar = full0 + 8 * stage;
       const int y0 = it.row_begin + t * TILE;
       const bool with_new = it.new_row >= y0 && it.new_row < y0 + TILE;
+      // the item's q rows and the unit's new rows (checked builds: only from
+      // inside their arrays, and only those bytes are expected)
+      const int h0 = it.hc * (HEADS > 0 ? HEADS : 1);
+      const int nh = HEADS > 0 ? min(HEADS, p.group - h0) : 0;
+      const size_t bhq = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0;
+      const bool load_q = HEADS > 0 && t == 0 && DA_IN(p, bhq + nh - 1, size_t(p.B) * p.h_q);
+      const size_t src = size_t(it.b) * p.h_kv + it.kvh;
+      const bool load_new = with_new && DA_IN(p, src, size_t(p.B) * p.h_kv);
       uint32_t extra = 0;
-      if (HEADS > 0 && t == 0) {
-        const int h0 = it.hc * HEADS;
-        const int nh = min(HEADS, p.group - h0);
-        extra += uint32_t(nh) * QROW;
-      }
-      if (with_new) extra += KROW + VROW;
+      if (load_q) extra += uint32_t(nh) * QROW;
+      if (load_new) extra += KROW + VROW;
       mbar_arrive_expect_tx(bar, STAGE_BYTES + extra);
-      if (HEADS > 0 && t == 0) {
-        const int h0 = it.hc * HEADS;
-        const int nh = min(HEADS, p.group - h0);
-        const char* qsrc = static_cast<const char*>(p.q) +
-                           (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * QROW;
-        bulk_load(qslots + stage * (HEADS * QROW), qsrc, uint32_t(nh) * QROW, bar);
-      }
-      if (with_new) {
-        const size_t src = size_t(it.b) * p.h_kv + it.kvh;
+      if (load_q)
+        bulk_load(qslots + stage * (HEADS * QROW), static_cast<const char*>(p.q) + bhq * QROW,
+                  uint32_t(nh) * QROW, bar);
+      if (load_new) {
         bulk_load(newslots + stage * kNewSlot, static_cast<const char*>(p.k_new) + src * KROW,
                   KROW, bar);
         bulk_load(newslots + stage * kNewSlot + KROW,

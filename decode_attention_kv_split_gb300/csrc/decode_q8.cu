@@ -192,15 +192,18 @@ __device__ __forceinline__ void produce_q8(const CUtensorMap* tmK, const CUtenso
       uint32_t extra = 0;
       const int h0 = it.hc * Cfg::kHeadsPerCta;
       const int nh = min(Cfg::kHeadsPerCta, p.group - h0);
-      if (t == 0) extra += uint32_t(nh) * (D * 2);
-      if (with_new) extra += 2 * D;
+      // (checked builds: q and new rows only from inside their arrays)
+      const size_t bhq = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0;
+      const bool load_q = t == 0 && DA_IN(p, bhq + nh - 1, size_t(p.B) * p.h_q);
+      const bool load_new = with_new && DA_IN(p, size_t(it.b) * p.h_kv + it.kvh, size_t(p.B) * p.h_kv);
+      if (load_q) extra += uint32_t(nh) * (D * 2);
+      if (load_new) extra += 2 * D;
       mbar_arrive_expect_tx(bar, Cfg::kStageBytes + extra);
-      if (t == 0) {
-        const char* qsrc = static_cast<const char*>(p.q) +
-                           (size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0) * (D * 2);
+      if (load_q) {
+        const char* qsrc = static_cast<const char*>(p.q) + bhq * (D * 2);
         bulk_load(qslots + stage * Cfg::kQBytes, qsrc, uint32_t(nh) * (D * 2), bar);
       }
-      if (with_new) {
+      if (load_new) {
         const size_t src = (size_t(it.b) * p.h_kv + it.kvh) * D;
         bulk_load(newslots + stage * Cfg::kNewBytes, static_cast<const char*>(p.k_new) + src, D,
                   bar);
@@ -425,7 +428,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       // the appended row goes into the caches once per kv head, by the warp that owns it
-      if (mine_new && it.hc == 0 && !*abort_flag) {
+      if (mine_new && it.hc == 0 && !*abort_flag &&
+          DA_IN(p, kvhead * size_t(p.n_max) + size_t(it.new_row), p.cache_rows)) {
         const size_t row_off = kvhead * size_t(p.n_max) + size_t(it.new_row);
         if (lane < D / 16) {
           reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + row_off * D)[lane] =
@@ -775,7 +779,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       // the appended row goes into the caches once per kv head, by the warp that owns it
-      if (new_local >= key0 && new_local < key0 + 16 && it.hc == 0 && !*abort_flag) {
+      if (new_local >= key0 && new_local < key0 + 16 && it.hc == 0 && !*abort_flag &&
+          DA_IN(p, kvhead * size_t(p.n_max) + size_t(it.new_row), p.cache_rows)) {
         const size_t row_off = kvhead * size_t(p.n_max) + size_t(it.new_row);
         if (lane < D / 16) {
           reinterpret_cast<uint4*>(static_cast<char*>(p.k_cache) + row_off * D)[lane] =

@@ -216,10 +216,11 @@ __device__ __forceinline__ void produce_ring(const CUtensorMap* map, const void*
       const uint32_t dst = slots + slot * TILE_BYTES;
       tma_load_3d(dst, map, 0, y0, z, bar, policy);
       tma_load_3d(dst + HALF_BYTES, map, 64, y0, z, bar, policy);
-      if (with_new)
-        bulk_load(newslots + slot * ROW_BYTES,
-                  static_cast<const char*>(new_rows) + (size_t(it.b) * p.h_kv + it.kvh) * ROW_BYTES,
-                  ROW_BYTES, bar);
+      if (with_new)  // (a checked build flags a row outside k_new / v_new and leaves the stage short)
+        if (DA_IN(p, size_t(it.b) * p.h_kv + it.kvh, size_t(p.B) * p.h_kv))
+          bulk_load(newslots + slot * ROW_BYTES,
+                    static_cast<const char*>(new_rows) + (size_t(it.b) * p.h_kv + it.kvh) * ROW_BYTES,
+                    ROW_BYTES, bar);
       issued |= 1u << slot;
       issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
       if (++slot == NSLOT) {
@@ -371,8 +372,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           for (int u = 0; u < kPerLane; ++u) {  // all loads in flight at once
             const int ch = lane + 32 * u;
             const int h = ch / (D / 8), c = (ch % (D / 8)) * 8;
-            v[u] = h0 + h < p.group ? __ldg(reinterpret_cast<const uint4*>(qbase + h * (D * 2) + c * 2))
-                                    : make_uint4(0, 0, 0, 0);
+            const size_t bhq = size_t(it.b) * p.h_q + size_t(it.kvh) * p.group + h0 + h;
+            v[u] = h0 + h < p.group && DA_IN(p, bhq, size_t(p.B) * p.h_q)
+                       ? __ldg(reinterpret_cast<const uint4*>(qbase + h * (D * 2) + c * 2))
+                       : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int u = 0; u < kPerLane; ++u) {
@@ -396,7 +399,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int ch = lane; ch < D / 8; ch += 32)
               *reinterpret_cast<uint4*>(kt + tc5::sw128(new_local, ch * 8, T)) =
                   reinterpret_cast<const uint4*>(slot)[ch];
-            if (it.hc == 0) {  // and into the K cache
+            if (it.hc == 0 &&  // and into the K cache
+                DA_IN(p, (size_t(p.b_offset + it.b) * p.h_kv + it.kvh) * size_t(p.n_max) + it.new_row,
+                      p.cache_rows)) {
               const size_t head = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
               uint4* dst = reinterpret_cast<uint4*>(
                   static_cast<char*>(p.k_cache) + (head * size_t(p.n_max) + size_t(it.new_row)) * (D * 2));
@@ -453,7 +458,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int ch = lane; ch < D / 8; ch += 32)
               *reinterpret_cast<uint4*>(vt + tc5::sw128(new_local, ch * 8, T)) =
                   reinterpret_cast<const uint4*>(slot)[ch];
-            if (it.hc == 0) {  // and into the V cache
+            if (it.hc == 0 &&  // and into the V cache
+                DA_IN(p, (size_t(p.b_offset + it.b) * p.h_kv + it.kvh) * size_t(p.n_max) + it.new_row,
+                      p.cache_rows)) {
               const size_t head = size_t(p.b_offset + it.b) * p.h_kv + it.kvh;
               uint4* dst = reinterpret_cast<uint4*>(
                   static_cast<char*>(p.v_cache) + (head * size_t(p.n_max) + size_t(it.new_row)) * (D * 2));
@@ -692,7 +699,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       for (int h = 0; h < HT; ++h)
         if (hb + h < nheads) {
           if (single) store_out(p, base + h * stride, o[h] * inv_l[h]);
-          else p.o_part[base + h * stride] = o[h] * inv_l[h];
+          else if (DA_IN(p, base + h * stride, p.part_rows * D))
+            p.o_part[base + h * stride] = o[h] * inv_l[h];
         }
       if ((!single || p.lse_out) && quarter == 0 && lane < HT && hb + lane < nheads) {
         float m_h = m_run[0], l_h = L[0];
@@ -703,8 +711,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             l_h = L[h];
           }
         const float lse2 = l_h > 0.f ? m_h + log2f(l_h) : -INFINITY;
-        if (!single) p.lse_part[(bh0 + hb + lane) * p.max_splits + it.split] = lse2;
-        else p.lse_out[bh0 + hb + lane] = lse2 * kLn2;
+        if (!single) {
+          if (DA_IN(p, (bh0 + hb + lane) * p.max_splits + it.split, p.part_rows))
+            p.lse_part[(bh0 + hb + lane) * p.max_splits + it.split] = lse2;
+        } else if (DA_IN(p, bh0 + hb + lane, size_t(p.B) * p.h_q)) {
+          p.lse_out[bh0 + hb + lane] = lse2 * kLn2;
+        }
       }
     }
     // the next item's first P.V overwrites O: our TMEM reads are complete

@@ -82,6 +82,8 @@ typedef enum {
 #define DA_DEVERR_SEQ_LEN 1 /* some seq_lens[b] outside [0, n_max]: clamped into range */
 #define DA_DEVERR_POS 2     /* some kv_append pos[b] outside [0, n_max): that row not written */
 #define DA_DEVERR_TIMEOUT 4 /* a pipeline wait exceeded its time limit: outputs invalid */
+#define DA_DEVERR_BOUNDS 8  /* bounds-checked test builds only: an index fell outside its
+                               buffer and that access was skipped; outputs invalid */
 
 /*
  * Supported sizes: d_k == d_v in {64, 128} for every cache type, and for

@@ -130,6 +130,7 @@ def test_header_constants_match_binding():
     assert int(defs["DA_DEVERR_SEQ_LEN"], 0) == api.DEVERR_SEQ_LEN
     assert int(defs["DA_DEVERR_POS"], 0) == api.DEVERR_POS
     assert int(defs["DA_DEVERR_TIMEOUT"], 0) == api.DEVERR_TIMEOUT
+    assert int(defs["DA_DEVERR_BOUNDS"], 0) == api.DEVERR_BOUNDS
 
 
 def test_no_fallback_when_library_missing(tmp_path, monkeypatch):

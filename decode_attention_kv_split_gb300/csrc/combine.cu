@@ -48,29 +48,16 @@ __device__ __forceinline__ void ldcg_vec(float (&v)[EPL], const float* src) {
   }
 }
 
-template <int D, int W>
-__global__ void __launch_bounds__(W * 32, 32 / W)
-    lse_combine_kernel(const SplitParams p, int heads_per_cta) {
-  constexpr int EPL = D / 32;
-  constexpr int kWarps = W;
-  extern __shared__ float csm[];
-  float* red_acc = csm;                 // [kWarps][D]
-  float* red_m = csm + kWarps * D;      // [kWarps]
-  float* red_w = red_m + kWarps;        // [kWarps]
-
-  // The next kernel on the stream may launch now: a split kernel's CTAs
-  // cannot share an SM with a combine CTA (registers), so they take the SMs
-  // this grid leaves free and wait there (griddepcontrol.wait) until it has
-  // completed, with their set-up done and no launch latency left.
-  allow_dependent_launch();
-  wait_for_prerequisite_grid();
-
+// Splits the split kernel wrote for query head bh = b * h_q + h: the same
+// rules as its work list (the rows decoded for sequence b, then the chunked
+// list's ceil(n / chunk) or, for balanced pieces, the count the unit's first
+// CTA recorded).  Returns 1 when the split kernel wrote the output itself and
+// 0 when a checked build finds the partial rows or the output row outside
+// their buffers.
+template <int D>
+__device__ __forceinline__ int combine_splits(const SplitParams& p, int bh, int heads_per_cta) {
   const int h_q = p.h_q;
-  const int bh = blockIdx.x;
   const int b = bh / h_q;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  // the rows the split kernel decoded for sequence b (same rules as its work list)
   int n = __ldg(p.seq_lens + b);
   const bool appended = p.append && n >= 0 && n < p.n_max;
   n = n < 0 ? 0 : (n > p.n_max ? p.n_max : n);
@@ -85,18 +72,30 @@ __global__ void __launch_bounds__(W * 32, 32 / W)
     const int kvh = h / group, hc = (h - kvh * group) / heads_per_cta;
     nv = __ldcg(p.unit_nv + (b * p.h_kv + kvh) * p.head_chunks + hc);
   }
-  if (nv <= 1) return;  // written by the split kernel
+  if (nv <= 1) return 1;
   // (checked builds: the partial rows and the output row stay inside their buffers)
   if (!DA_IN(p, size_t(bh) * p.max_splits + nv - 1, p.part_rows) ||
       !DA_IN(p, size_t(bh) * D + D - 1, p.out_elems))
-    return;  // CTA-uniform
+    return 0;
+  return nv;
+}
+
+// Merge of one query head's nv > 1 partials by the whole CTA.  Warp w takes
+// splits w, w + kWarps, ... in passes of NB splits in flight (vector loads
+// from L2), keeping a running maximum of the lse values it has seen (the
+// online form of the combine: every weight is taken against the same maximum
+// that scales the warp's sum).  Each lane holds D/32 consecutive columns.  The
+// warp results meet in shared memory and are merged the same way; the output
+// row and the head's natural-log lse are written.
+template <int D, int kWarps, int NB>
+__device__ __forceinline__ void merge_head(const SplitParams& p, int bh, int nv, float* red_acc,
+                                           float* red_m, float* red_w) {
+  constexpr int EPL = D / 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const float* lse = p.lse_part + size_t(bh) * p.max_splits;
   const float* op = p.o_part + size_t(bh) * p.max_splits * D + lane * EPL;
 
-  // NB splits per warp in flight at once (vector loads from L2): one pass
-  // covers NB * kWarps splits, 272 for d <= 128 (256 splits and the one that
-  // rows appended past n_max open).
-  constexpr int NB = EPL == 4 ? 17 : (EPL == 2 ? 16 : 8);
   float m = -INFINITY, wsum = 0.f, acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
@@ -154,6 +153,33 @@ __global__ void __launch_bounds__(W * 32, 32 / W)
     else static_cast<float*>(p.out)[size_t(bh) * D + d] = v;
     if (d == 0 && p.lse_out) p.lse_out[bh] = W > 0.f ? (M_use + log2f(W)) * kLn2 : -INFINITY;
   }
+}
+
+template <int D, int W>
+__global__ void __launch_bounds__(W * 32, 32 / W)
+    lse_combine_kernel(const SplitParams p, int heads_per_cta) {
+  constexpr int EPL = D / 32;
+  constexpr int kWarps = W;
+  extern __shared__ float csm[];
+  float* red_acc = csm;                 // [kWarps][D]
+  float* red_m = csm + kWarps * D;      // [kWarps]
+  float* red_w = red_m + kWarps;        // [kWarps]
+
+  // The next kernel on the stream may launch now: a split kernel's CTAs
+  // cannot share an SM with a combine CTA (registers), so they take the SMs
+  // this grid leaves free and wait there (griddepcontrol.wait) until it has
+  // completed, with their set-up done and no launch latency left.
+  allow_dependent_launch();
+  wait_for_prerequisite_grid();
+
+  const int bh = blockIdx.x;
+  const int nv = combine_splits<D>(p, bh, heads_per_cta);
+  if (nv <= 1) return;  // written by the split kernel, or out of range (CTA-uniform)
+  // NB splits per warp in flight at once: one pass covers NB * kWarps
+  // splits, 272 for d <= 128 (256 splits and the one that rows appended past
+  // n_max open).
+  constexpr int NB = EPL == 4 ? 17 : (EPL == 2 ? 16 : 8);
+  merge_head<D, kWarps, NB>(p, bh, nv, red_acc, red_m, red_w);
 }
 
 template <int D, int W>

@@ -581,6 +581,62 @@ __device__ __forceinline__ int choose_chunk(const SplitParams& p, const int* len
   return red[kSchedRedWords - 1];
 }
 
+// The same choice made by one warp for a launch slice of at most 32
+// sequences: lane b holds n_b (0 for lanes past the batch), and lane k
+// evaluates candidate k over every sequence by shuffles, so the choice needs
+// no barrier.  `rows` and `nmax` are the slice's row total and longest length,
+// the same on every lane.  Every lane returns the chosen length.
+template <int TILE>
+__device__ __forceinline__ int choose_chunk_warp(const SplitParams& p, int n_lane, int grid,
+                                                 float rows, int nmax) {
+  const int k = threadIdx.x & 31;
+  const int longest = nmax > 0 ? nmax : 1;
+  const int per_seq = p.h_kv * p.head_chunks;
+  const int units = p.B * per_seq;
+  uint32_t c;  // candidate length, as in choose_chunk
+  if (k < 16) {
+    const unsigned long long c64 = (unsigned long long)p.chunk_min << k;
+    c = c64 > (1ull << 30) ? (1u << 30) : uint32_t(c64);
+  } else {
+    int pieces = (k - 15) * grid / units;
+    if (pieces < 1) pieces = 1;
+    c = uint32_t(longest / pieces + (longest % pieces != 0));
+  }
+  c = (c + TILE - 1) / TILE * TILE;
+  if (c < uint32_t(p.chunk_min)) c = uint32_t(p.chunk_min);
+  if (c > (1u << 30)) c = 1u << 30;
+  const int ci = int(c);
+  const bool candidate = k >= 16 || k == 0 || ((long long)p.chunk_min << (k - 1)) < longest;
+  long long all = 0;
+  for (int b = 0; b < p.B; ++b) {  // warp-uniform bound
+    const int n = __shfl_sync(0xffffffffu, n_lane, b);
+    all += n <= 0 ? 1 : (n - 1) / ci + 1;
+  }
+  float t = 3.0e38f;
+  if (candidate) {
+    const float fitems = float(all) * float(per_seq);
+    const float rounds = ceilf(fitems / float(grid));
+    const float share = rows * float(per_seq) / float(grid);
+    const float ceff = float(ci < longest ? ci : longest);
+    t = fmaxf(share, rounds * ceff / p.cta_speed) + rounds * float(TILE);
+    if (ci < longest) t += 2.f * float(TILE);
+  }
+  float best_t = t;
+  int best_c = ci;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // argmin; within 0.1% the shorter length
+    const float ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+    const int oc = __shfl_xor_sync(0xffffffffu, best_c, o);
+    const bool take = oc < best_c ? ot <= best_t * 1.001f
+                                  : (oc == best_c ? false : ot * 1.001f < best_t);
+    if (take) {
+      best_t = ot;
+      best_c = oc;
+    }
+  }
+  return best_c;
+}
+
 // The rows a sequence contributes to the work list, from its seq_lens value:
 // clamped into [0, n_max], plus the appended row when there is room for it
 // (kAppendFlag set), else cut to the decoded row range.  `n_out` receives the
@@ -621,6 +677,7 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
   bool bad_pos = false;
   float rows = 0.f;  // only feeds the split-length model; summed in a fixed order
   int nmax = 0;
+  int my_n = 0;      // n of sequence tid (the one-warp path: B <= 32)
   for (int b = tid; b < p.B; b += blockDim.x) {
     int n_out;
     const int lv = list_len(p, __ldcg(p.seq_lens + b), bad, bad_pos, n_out);  // through L2
@@ -628,6 +685,7 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
     lens[b] = lv;
     rows += float(n);
     nmax = n > nmax ? n : nmax;
+    my_n = n;
   }
   (void)bad, (void)bad_pos;
   Schedule s;
@@ -694,7 +752,36 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
     __syncthreads();
     return s;
   }
-  if (p.chunk_fixed > 0) {
+  if (p.B <= 32) {
+    // One warp: the split length, then the scan of the full splits per
+    // sequence, with shuffles only; the other warps wait at one barrier.
+    if (warp == 0) {
+      float wrows = rows;
+      int wmax = nmax;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        wrows += __shfl_xor_sync(0xffffffffu, wrows, o);
+        wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      }
+      const int chunk = p.chunk_fixed > 0
+                            ? p.chunk_fixed
+                            : choose_chunk_warp<TILE>(p, my_n, gridDim.x, wrows, wmax);
+      const int c = lane < p.B ? per_seq * (my_n <= 0 ? 0 : (my_n - 1) / chunk) : 0;
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane < p.B) first[lane] = x - c;
+      if (lane == 31) {
+        first[p.B] = x;
+        red[kSchedRedWords - 1] = chunk;
+      }
+    }
+    __syncthreads();
+    s.chunk = red[kSchedRedWords - 1];
+  } else if (p.chunk_fixed > 0) {
     __syncthreads();
     s.chunk = p.chunk_fixed;
   } else {
@@ -718,7 +805,7 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
     s.chunk = choose_chunk<TILE>(p, lens, gridDim.x, all_rows, all_max, red);
   }
   // exclusive scan of the full-split items per sequence by warp 0
-  if (tid < 32) {
+  if (p.B > 32 && tid < 32) {
     int carry = 0;
     for (int base = 0; base < p.B; base += 32) {
       const int b = base + tid;
@@ -738,7 +825,7 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
     }
     if (tid == 0) first[p.B] = carry;
   }
-  __syncthreads();
+  if (p.B > 32) __syncthreads();
   s.total = first[p.B] + per_seq * p.B;  // and one last split per unit
   // decode this CTA's first items, one per thread
   const int mine = s.total > int(blockIdx.x) ? (s.total - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
@@ -911,11 +998,23 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
 // This CTA's hint from the previous launch, if it is well formed and inside
 // this launch's tensors: rows [y0, y0 + tiles * TILE) of kv head z.  Called
 // before griddepcontrol.wait: the words may be stale, never unsafe to use.
+// The hint word of this CTA, loaded through L2 without waiting for it: the
+// caller issues the load at kernel entry and decodes the value once the work
+// list is built, so the load's round trip overlaps the build.
+__device__ __forceinline__ int4 load_hint(const SplitParams& p) {
+  int4 h = make_int4(0, 0, 0, 0);
+  if (p.hints && blockIdx.x < unsigned(kMaxHintCtas))
+    asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(h.x), "=r"(h.y), "=r"(h.z), "=r"(h.w)
+                 : "l"(p.hints + blockIdx.x));
+  return h;
+}
+
+// A hint word written by write_hint for this launch's shapes: its first tiles.
 template <int TILE>
-__device__ __forceinline__ bool read_hint(const SplitParams& p, int max_tiles, int& z, int& y0,
-                                          int& tiles) {
+__device__ __forceinline__ bool read_hint(const SplitParams& p, int4 h, int max_tiles, int& z,
+                                          int& y0, int& tiles) {
   if (!p.hints || blockIdx.x >= unsigned(kMaxHintCtas)) return false;
-  const int4 h = __ldcg(p.hints + blockIdx.x);
   z = h.x, y0 = h.y, tiles = h.z;
   if ((h.x ^ h.y ^ h.z ^ kHintSeal) != h.w) return false;
   const int z0 = p.b_offset * p.h_kv, z1 = (p.b_offset + p.B) * p.h_kv;
@@ -937,10 +1036,11 @@ __device__ __forceinline__ void write_hint(const SplitParams& p, const Item& it,
 // Producer lane, before waiting for the previous grid: L2 prefetch of the
 // hinted tiles of K (NBOX_K boxes of BOX_COLS columns per tile) and V.
 template <int TILE, int NBOX_K, int NBOX_V, int BOX_COLS>
-__device__ __forceinline__ void prefetch_hinted(const SplitParams& p, const CUtensorMap* tmK,
-                                                const CUtensorMap* tmV, int max_tiles) {
+__device__ __forceinline__ void prefetch_hinted(const SplitParams& p, int4 hint,
+                                                const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                                int max_tiles) {
   int z, y0, tiles;
-  if (!read_hint<TILE>(p, max_tiles, z, y0, tiles)) return;
+  if (!read_hint<TILE>(p, hint, max_tiles, z, y0, tiles)) return;
   for (int t = 0; t < tiles && y0 + t * TILE < p.n_max; ++t) {
 #pragma unroll
     for (int h = 0; h < NBOX_K; ++h) tma_prefetch_3d(tmK, h * BOX_COLS, y0 + t * TILE, z);

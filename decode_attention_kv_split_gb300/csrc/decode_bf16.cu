@@ -112,15 +112,19 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
-  if (threadIdx.x == Cfg::kConsumerThreads)  // producer lane: L2 prefetch of the hinted tiles
-    prefetch_hinted<Cfg::kTile, Cfg::kHalvesK, Cfg::kHalvesV, 64>(p, &tmK, &tmV, STAGES);
-  // Launched as a programmatic dependent: the set-up above overlaps the tail
+  int4 hint = make_int4(0, 0, 0, 0);
+  if (threadIdx.x == Cfg::kConsumerThreads) hint = load_hint(p);  // producer lane
+  // Launched as a programmatic dependent: the set-up here overlaps the tail
   // of the previous grid on the stream, which may have produced seq_lens, q,
   // the caches or the new rows.  Before the wait below, only the hinted L2
   // prefetch and the work list touch them: the prefetch is a hint, and the
   // list is built on the lengths as they read now (shared memory only), then
-  // checked and built again if they changed once the wait is over.
+  // checked and built again if they changed once the wait is over.  The hint
+  // is loaded first and used after the build, so that its round trip does
+  // not hold the build's first barrier.
   Schedule sched = build_schedule_core<Cfg::kTile>(p, sched_words);
+  if (threadIdx.x == Cfg::kConsumerThreads)
+    prefetch_hinted<Cfg::kTile, Cfg::kHalvesK, Cfg::kHalvesV, 64>(p, hint, &tmK, &tmV, STAGES);
   wait_for_prerequisite_grid();
   sched = commit_schedule<Cfg::kTile>(p, sched_words, sched);
   allow_dependent_launch();

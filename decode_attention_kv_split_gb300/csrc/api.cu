@@ -447,7 +447,7 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     if (err != cudaSuccess) return fail_cuda(err, "split kernel launch");
     g_launches.fetch_add(1);
     if (wl.total) {
-      err = da::launch_combine(p, d_v, pl.ks.heads_per_cta, stream);
+      err = da::launch_combine(p, d_v, pl.ks.heads_per_cta, grid, stream);
       if (err != cudaSuccess) return fail_cuda(err, "combine kernel launch");
       g_launches.fetch_add(1);
     }

@@ -295,7 +295,10 @@ cudaError_t launch_split_bf16(const SplitParams& p, const CUtensorMap& tk, const
                               int d_k, int d_v, int grid, cudaStream_t stream);
 cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              int d, int grid, cudaStream_t stream);
-cudaError_t launch_combine(const SplitParams& p, int d, int heads_per_cta, cudaStream_t stream);
+// split_grid: the CTAs of the split launch before it (the expected pieces per
+// unit of a balanced list).
+cudaError_t launch_combine(const SplitParams& p, int d, int heads_per_cta, int split_grid,
+                           cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, void* out,
                              int out_bf16, float* lse_out, long long heads, int d,
                              cudaStream_t stream);

@@ -250,7 +250,7 @@ bool single_split_suffices(long long units, int n_max, int chunk_min, int tile, 
 // lengths; the host only bounds it from below so that the partial outputs of
 // at most about 4 x SMs work items per launch need workspace.
 int make_plan(int B, int h_q, int h_kv, int d, int d_v, int n_max, int dtype_arg, int requested,
-              int sms, Plan* pl) {
+              int sms, Plan* pl, bool balance_rule = true) {
   const int dtype = dtype_arg & 0xff;
   const int group = h_q / h_kv;
   pl->tc5 = dtype == DA_BF16 && d == 128 && d_v == 128 && group > 8;
@@ -265,20 +265,21 @@ int make_plan(int B, int h_q, int h_kv, int d, int d_v, int n_max, int dtype_arg
   pl->balanced = false;
   pl->units = int((long long)pl->batch_per_launch * h_kv * pl->head_chunks);
   if (requested < -1) return DA_ERR_SHAPE;
-  if (requested == -1) {
-    // Balanced pieces when the row stream fits an int and the partials of up
-    // to one per SM per query head stay within 256 MiB; otherwise the
-    // library's usual choice.
+  // Balanced pieces when the row stream fits an int and the partials of up
+  // to one per SM per query head stay within 256 MiB.
+  auto take_balanced = [&]() {
     const long long stream_rows = (long long)pl->units * n_max;
     const long long part_bytes = (long long)pl->batch_per_launch * h_q * sms * (d_v + 1) * 4;
-    if (stream_rows < (1LL << 31) && part_bytes <= (256LL << 20)) {
-      pl->balanced = true;
-      pl->chunk_fixed = 0;
-      pl->chunk_min = int(tile);
-      pl->max_splits = sms;  // a unit has at most one piece per CTA
-      return DA_OK;
-    }
-    requested = 0;
+    if (stream_rows >= (1LL << 31) || part_bytes > (256LL << 20)) return false;
+    pl->balanced = true;
+    pl->chunk_fixed = 0;
+    pl->chunk_min = int(tile);
+    pl->max_splits = sms;  // a unit has at most one piece per CTA
+    return true;
+  };
+  if (requested == -1) {
+    if (take_balanced()) return DA_OK;
+    requested = 0;  // otherwise the library's usual choice
   }
   if (requested > 0) {
     long long tiles = (n_max + (long long)requested * tile / 2) / ((long long)requested * tile);
@@ -294,6 +295,15 @@ int make_plan(int B, int h_q, int h_kv, int d, int d_v, int n_max, int dtype_arg
     pl->chunk_fixed = 0;
     pl->chunk_min = int((per + tile - 1) / tile * tile);
     if (single_split_suffices(units, n_max, pl->chunk_min, int(tile), sms, pl->ks.cta_speed)) {
+      // One split per unit needs no partials and no combine, but when the
+      // units fill the grid's rounds unevenly (fewer units than CTAs, or a
+      // ragged last round) the CTAs without a unit idle while the longest
+      // sequences stream.  Then balanced pieces, if each CTA's share is at
+      // least 8 tiles (below that the merge costs more than the idle SMs).
+      const long long rounds = (units + sms - 1) / sms;
+      const bool uneven = double(units) < 0.9 * double(rounds * sms);
+      const bool sizeable = units * (long long)n_max >= 8LL * tile * sms;
+      if (balance_rule && uneven && sizeable && take_balanced()) return DA_OK;
       pl->chunk_fixed = int(max_tiles * tile);  // one split: no partials, no combine
       pl->chunk_min = pl->chunk_fixed;
     }
@@ -457,6 +467,19 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
 
 
 }  // namespace
+
+namespace da {
+// Whether the library's own split choice (num_splits = 0) takes balanced
+// pieces by the uneven-grid rule of make_plan for this request.
+bool library_takes_balanced(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype) {
+  if (check_sizes(B, h_q, h_kv, d_k, d_v, n_max, dtype) != DA_OK) return false;
+  int dev = 0, sms = 0;
+  if (current_device(&dev, &sms) != DA_OK) return false;
+  Plan pl;
+  if (make_plan(B, h_q, h_kv, d_k, d_v, n_max, dtype, 0, sms, &pl) != DA_OK) return false;
+  return pl.balanced;
+}
+}  // namespace da
 
 extern "C" {
 

@@ -297,6 +297,11 @@ cudaError_t launch_split_f32(const SplitParams& p, const CUtensorMap& tk, const 
                              int d, int grid, cudaStream_t stream);
 // split_grid: the CTAs of the split launch before it (the expected pieces per
 // unit of a balanced list).
+// Host: whether num_splits = 0 resolves to balanced pieces for this request
+// (the allocation-free entry point takes one split instead when those pieces'
+// partials do not fit its buffer).
+bool library_takes_balanced(int B, int h_q, int h_kv, int d_k, int d_v, int n_max, int dtype);
+
 cudaError_t launch_combine(const SplitParams& p, int d, int heads_per_cta, int split_grid,
                            cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int S, void* out,

@@ -104,9 +104,16 @@ extern "C" int decode_attn_noalloc(const void* q, const void* K, const void* V,
                                    int num_splits, int32_t* dev_error, cudaStream_t stream) {
   if (!q || !K || !V || !seq_lens || !out) return DA_ERR_NULL;
   int st = DA_OK;
-  const size_t need = decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype,
-                                                  num_splits, &st);
+  size_t need = decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype, num_splits,
+                                            &st);
   if (st != DA_OK) return st;
+  if (need > kNoAllocScratchBytes && num_splits == 0 &&
+      da::library_takes_balanced(B, h_q, h_kv, d_k, d_v, n_max, dtype)) {
+    // the library's balanced pieces do not fit: one split per sequence instead
+    num_splits = 1;
+    need = decode_attn_workspace_bytes(B, h_q, h_kv, d_k, d_v, n_max, dtype, num_splits, &st);
+    if (st != DA_OK) return st;
+  }
   if (need > kNoAllocScratchBytes) return DA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {

@@ -124,7 +124,11 @@ DA_API size_t decode_attn_workspace_bytes(int B, int h_q, int h_kv, int d_k, int
  *   seq_lens     : device int32 [B]; 0 <= seq_lens[b] <= n_max.  Values out
  *                  of range are clamped and flagged in *dev_error.
  *   scale        : multiplies q.K (typically 1/sqrt(d_k)).
- *   num_splits   : splits per (b, kv head); 0 = library's choice; -1 =
+ *   num_splits   : splits per (b, kv head); 0 = library's choice (equal
+ *                  splits whose length the kernels pick from the lengths,
+ *                  one split per unit, or balanced pieces when one split per
+ *                  unit would leave more than a tenth of the grid's rounds
+ *                  idle and each CTA's share is at least 8 tiles); -1 =
  *                  balanced: the rows of all (sequence, kv head) units, unit
  *                  after unit, are cut into one equal piece per SM (at tile
  *                  boundaries), for batches whose lengths differ widely (the
@@ -202,7 +206,9 @@ DA_API int decode_attn(const void* q, const void* K, const void* V, const int32_
  * need less).  Balanced pieces (num_splits = -1) keep up to one partial per
  * SM per query head, which exceeds the buffer for all but small batches
  * (B = 16, h_q = 32, d_v = 128 already needs ~39 MB): such requests are
- * rejected, not served with another split choice.  Calls no cudaMalloc,
+ * rejected, not served with another split choice.  When the library's own
+ * choice (num_splits = 0) is balanced pieces that do not fit, the call takes
+ * one split per sequence instead (as num_splits = 1 would).  Calls no cudaMalloc,
  * cudaFree or other allocating routine.  The first call on a device looks up
  * the buffer's device address with that device current and caches it with
  * the id of the device's current context (a call after cudaDeviceReset looks

@@ -331,6 +331,27 @@ def test_balanced_pieces_ragged(o, case):
     check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_library_choice_balances_an_uneven_grid(o, dtype):
+    """With the library's choice, where one split per unit would be taken but
+    the units leave much of the grid idle (16 sequences x 8 kv heads = 128
+    units on 152 CTAs), the units get balanced pieces instead; units that fill
+    whole rounds keep one split each."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, h_q, h_kv, d, n_max = 16, 32, 8, 128, 4096
+    if 128 >= 0.9 * sms:
+        pytest.skip("128 units fill this device's grid")
+    assert api.resolve_splits(B, h_q, h_kv, d, d, n_max, dtype, 0) == sms
+    if sms % 8 == 0:  # sms / 8 sequences x 8 kv heads: exactly one round of units
+        assert api.resolve_splits(sms // 8, h_q, h_kv, d, d, n_max, dtype, 0) == 1
+    rng = np.random.default_rng(12)
+    lens = [int(x) for x in rng.integers(1, n_max + 1, B)]
+    lens[0] = n_max
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=12)
+    out = gpu_decode(q, K, V, lens_t, num_splits=0)
+    check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
 # ----------------------------------------------------------------- fused append + decode
 def _bits(t):
     return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).numpy()

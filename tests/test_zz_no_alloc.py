@@ -99,3 +99,21 @@ def test_noalloc_rejects_requests_beyond_its_scratch(lib):
     assert st == -5   # DA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert all(bool((t == 0).all()) for t in bufs)
+
+
+def test_noalloc_takes_one_split_when_balanced_pieces_do_not_fit(lib):
+    """The library's choice here is balanced pieces (128 units on a 152-SM grid),
+    whose partials (~40 MB) exceed the buffer: the call takes one split per
+    sequence instead, exactly as num_splits = 1 computes it."""
+    B, h_q, h_kv, d, n_max = 16, 32, 8, 128, 8192
+    lens = [8192, 1024, 5000, 7777, 3000, 8191, 1500, 6000, 2048, 4096, 100, 8000, 512, 7000, 2500, 6500]
+    if api.resolve_splits(B, h_q, h_kv, d, d, n_max, torch.bfloat16, 0) <= 1:
+        pytest.skip("the library takes one split on this device's grid")
+    assert api.workspace_bytes(B, h_q, h_kv, d, d, n_max, torch.bfloat16, 0) > SCRATCH_LIMIT
+    q, K, V, lens_t, scale = _inputs(B, h_q, h_kv, d, n_max, lens, torch.bfloat16, seed=7)
+    ref = api.decode_attn(q, K, V, lens_t, scale=scale, num_splits=1)
+    out = torch.full_like(ref, float("nan"))
+    st = _call_noalloc(lib, q, K, V, lens_t, out, scale, 0)
+    assert st == 0, lib.decode_attn_status_string(st).decode()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)

@@ -452,9 +452,11 @@ __device__ __forceinline__ uint32_t bal_cut(const SplitParams& p, const Schedule
   return start + (x - start) / TILE * TILE;
 }
 
-// The item of CTA c on unit u.
+// The item of CTA c on unit u (inlined into the work-list build, where it is
+// on every CTA's start-up path; bal_item_far below is the out-of-line copy for
+// items decoded on the fly past the item cache).
 template <int TILE>
-__device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, int c, int u) {
+__device__ __forceinline__ Item bal_item(const SplitParams& p, const Schedule& s, int c, int u) {
   const int per_seq = p.h_kv * p.head_chunks;
   const int b = u / per_seq, j = u - (u / per_seq) * per_seq;
   const uint32_t len = uint32_t(bal_len(s, b));
@@ -486,12 +488,17 @@ __device__ __noinline__ Item bal_item(const SplitParams& p, const Schedule& s, i
   return it;
 }
 
+template <int TILE>
+__device__ __noinline__ Item bal_item_far(const SplitParams& p, const Schedule& s, int c, int u) {
+  return bal_item<TILE>(p, s, c, u);
+}
+
 // The k-th item of this CTA (k < s.mine), read back from shared memory when
 // build_schedule decoded it.
 template <int TILE>
 __device__ __forceinline__ Item cta_item(const SplitParams& p, const Schedule& s, int k) {
   if (k >= kItemCache)
-    return s.balanced ? bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + k)
+    return s.balanced ? bal_item_far<TILE>(p, s, int(blockIdx.x), s.u0 + k)
                       : schedule_item<TILE>(p, s, int(blockIdx.x) + k * int(gridDim.x));
   const int* w = s.w + kSchedItems + k * kItemWords;
   Item it;

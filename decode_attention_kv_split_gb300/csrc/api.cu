@@ -445,9 +445,9 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     p.withhold_cta = b0 == 0 ? g_test_withhold_cta.load() : -1;
 #endif
     const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
-    // one persistent CTA per SM (the balanced list keeps one boundary per CTA in
-    // the work list's reduction scratch)
-    const long long grid_cap = sms < da::kSchedRedWords - 1 ? sms : da::kSchedRedWords - 1;
+    // one persistent CTA per SM (the balanced list keeps a boundary and a unit
+    // tag per CTA in the two halves of the work list's reduction scratch)
+    const long long grid_cap = sms < da::kSchedRedWords / 2 - 1 ? sms : da::kSchedRedWords / 2 - 1;
     const int grid = int(items < grid_cap ? items : grid_cap);
     cudaError_t err =
         pl.tc5 ? da::launch_split_tc5(p, tk, tv, grid, stream)

@@ -440,16 +440,28 @@ __device__ __forceinline__ int bal_unit(const SplitParams& p, const Schedule& s,
   return int(uint32_t(lo) * per_seq + j);
 }
 
-// Stream position of boundary c (0 .. gridDim.x).
+// Stream position of boundary c (0 .. gridDim.x), and in `tag` the unit that
+// holds the rows from it on, times 2, plus 1 when the boundary is that unit's
+// first row (for the last boundary: the unit count, times 2, plus 1).
 template <int TILE>
-__device__ __forceinline__ uint32_t bal_cut(const SplitParams& p, const Schedule& s, int c) {
-  const uint32_t R = uint32_t(p.h_kv * p.head_chunks) * uint32_t(s.first(p.B));
+__device__ __forceinline__ uint32_t bal_cut(const SplitParams& p, const Schedule& s, int c,
+                                            int& tag) {
+  const uint32_t per_seq = uint32_t(p.h_kv * p.head_chunks);
+  const uint32_t R = per_seq * uint32_t(s.first(p.B));
   const uint32_t x = uint32_t(c) * uint32_t(s.piece);
-  if (c <= 0) return 0;
-  if (x >= R) return R;
+  if (c <= 0) {
+    tag = 1;  // unit 0, at its first row
+    return 0;
+  }
+  if (x >= R) {
+    tag = int(per_seq * uint32_t(p.B)) * 2 + 1;  // past the last unit
+    return R;
+  }
   uint32_t start;
-  bal_unit(p, s, x, start);
-  return start + (x - start) / TILE * TILE;
+  const int u = bal_unit(p, s, x, start);
+  const uint32_t cut = start + (x - start) / TILE * TILE;
+  tag = u * 2 + (cut == start ? 1 : 0);
+  return cut;
 }
 
 // The item of CTA c on unit u (inlined into the work-list build, where it is
@@ -737,18 +749,21 @@ __device__ __forceinline__ Schedule build_schedule_core(const SplitParams& p, in
     uint32_t piece = (R + gridDim.x - 1) / gridDim.x;
     if (piece < TILE) piece = TILE;  // so that no two boundaries round to the same row
     s.piece = int(piece);
-    // every boundary once, a thread each, into the reduction scratch
-    // (gridDim.x + 1 <= kSchedRedWords words; the host launches at most that many CTAs)
+    // every boundary once, a thread each, into the reduction scratch: the
+    // positions in its first half, the tags in its second (gridDim.x + 1 <=
+    // kSchedRedWords / 2 words each; the host launches at most that many CTAs)
+    int* tags = red + kSchedRedWords / 2;
     for (int c = tid; c <= int(gridDim.x); c += blockDim.x)
-      if (DA_IN(p, c, kSchedRedWords)) red[c] = int(bal_cut<TILE>(p, s, c));
+      if (DA_IN(p, c, kSchedRedWords / 2)) red[c] = int(bal_cut<TILE>(p, s, c, tags[c]));
     __syncthreads();
     s.cuts = red;
     const uint32_t lo = uint32_t(s.cuts[blockIdx.x]);
     const uint32_t hi = uint32_t(s.cuts[blockIdx.x + 1]);
     if (lo < hi) {
-      uint32_t start;
-      s.u0 = bal_unit(p, s, lo, start);
-      s.mine = bal_unit(p, s, hi - 1, start) - s.u0 + 1;
+      s.u0 = tags[blockIdx.x] >> 1;  // the unit of row lo
+      // the unit of row hi - 1: the one before hi's when hi is a unit's first row
+      const int th = tags[blockIdx.x + 1];
+      s.mine = (th >> 1) - (th & 1) - s.u0 + 1;
     }
     for (int t = tid; t < s.mine && t < kItemCache; t += blockDim.x) {
       const Item it = bal_item<TILE>(p, s, int(blockIdx.x), s.u0 + t);

@@ -352,6 +352,20 @@ def test_library_choice_balances_an_uneven_grid(o, dtype):
     check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_balanced_long_unit_among_short_ones(o, d):
+    """Balanced pieces over many short units and one long one: the combine is
+    the one-warp-per-head kind (few pieces per unit on average), and the long
+    unit's heads have many more pieces than one pass of it holds."""
+    B, h_q, h_kv, n_max = 64, 8, 2, 16384
+    lens = [64 + (7 * b) % 61 for b in range(B)]
+    lens[5] = n_max
+    dtype = torch.bfloat16
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, lens, dtype, seed=d)
+    out = gpu_decode(q, K, V, lens_t, num_splits=-1)
+    check_against_oracle(o, q, K, V, lens_t, scale, out, TOL[dtype])
+
+
 # ----------------------------------------------------------------- fused append + decode
 def _bits(t):
     return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).numpy()

@@ -447,7 +447,8 @@ int run_decode(const void* q, const void* K, const void* V, const int32_t* seq_l
     const long long items = (long long)bn * h_kv * pl.head_chunks * pl.max_splits;
     // one persistent CTA per SM (the balanced list keeps a boundary and a unit
     // tag per CTA in the two halves of the work list's reduction scratch)
-    const long long grid_cap = sms < da::kSchedRedWords / 2 - 1 ? sms : da::kSchedRedWords / 2 - 1;
+    const long long max_grid = da::kSchedRedWords / 2 - 1;
+    const long long grid_cap = sms < max_grid ? sms : max_grid;
     const int grid = int(items < grid_cap ? items : grid_cap);
     cudaError_t err =
         pl.tc5 ? da::launch_split_tc5(p, tk, tv, grid, stream)

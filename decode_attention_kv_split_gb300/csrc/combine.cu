@@ -49,11 +49,11 @@ __device__ __forceinline__ void ldcg_vec(float (&v)[EPL], const float* src) {
 }
 
 // Splits the split kernel wrote for query head bh = b * h_q + h, given the
-// sequence's seq_lens value: the same rules as its work list (the rows decoded for sequence b, then the chunked
-// list's ceil(n / chunk) or, for balanced pieces, the count the unit's first
-// CTA recorded).  Returns 1 when the split kernel wrote the output itself and
-// 0 when a checked build finds the partial rows or the output row outside
-// their buffers.
+// sequence's seq_lens value: the same rules as its work list (the rows
+// decoded for sequence b, then the chunked list's ceil(n / chunk) or, for
+// balanced pieces, the count the unit's first CTA recorded).  Returns 1 when
+// the split kernel wrote the output itself and 0 when a checked build finds
+// the partial rows or the output row outside their buffers.
 template <int D>
 __device__ __forceinline__ int splits_of_head(const SplitParams& p, int bh, int seq_len,
                                               int heads_per_cta) {
@@ -188,10 +188,11 @@ __global__ void __launch_bounds__(W * 32, 32 / W)
   merge_head<D, kWarps, NB>(p, bh, nv, red_acc, red_m, red_w);
 }
 
-// Warp-per-head combine, for heads with few splits.  Eight warps per CTA, one query head each, at most 64
-// registers a thread and no shared memory, so that four CTAs share an SM:
-// launched early, the grid waits on the first SMs the split grid frees and
-// holds as few of them as it can from the next call's split CTAs.  The
+// Warp-per-head combine, for heads with few splits.  Eight warps per CTA, one
+// query head each, at most 64 registers a thread and no shared memory, so
+// that four CTAs share an SM: launched early, the grid waits on the first SMs
+// the split grid frees and holds as few of them as it can from the next
+// call's split CTAs.  The
 // sequence's length is read before the wait (the split grid read the same
 // final value before it let this grid launch); after the wait the split count
 // and the first NB splits' partials are loaded together (slots past the count

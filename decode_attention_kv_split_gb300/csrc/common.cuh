@@ -185,6 +185,20 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// L2 policy for data a later kernel reads back soon (the split partials,
+// which the combine merges after the K/V stream has passed through L2).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// A float store that asks L2 to keep the line (policy from l2_policy_evict_last).
+__device__ __forceinline__ void st_keep(float* addr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -969,7 +983,7 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
       const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
       if (!single) {
         if (DA_IN(p, (bh0 + h) * p.max_splits + it.split, p.part_rows))
-          p.lse_part[(bh0 + h) * p.max_splits + it.split] = lse2;
+          st_keep(p.lse_part + (bh0 + h) * p.max_splits + it.split, lse2, l2_policy_evict_last());
       } else if (p.lse_out && DA_IN(p, bh0 + h, p.out_elems / D)) {
         p.lse_out[bh0 + h] = lse2 * kLn2;
       }
@@ -978,6 +992,7 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
   named_bar_sync(1, nthreads);
   const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
   const size_t base = single ? bh0 * D : (bh0 * p.max_splits + it.split) * D;
+  const uint64_t keep = l2_policy_evict_last();  // partials: read back by the combine
   for (int idx = ctid; idx < nh * D; idx += nthreads) {
     const int h = idx / D, d = idx - h * D;
     const int hg = h / HPW, hw = h - hg * HPW;
@@ -990,7 +1005,8 @@ __device__ __forceinline__ void finish_item(const SplitParams& p, const Item& it
     const float val = sum * epi_l[(hg * KW + 1) * HPW + hw];
     if (!*abort_flag) {
       if (single) store_out(p, base + h * stride + d, val);
-      else if (DA_IN(p, base + h * stride + d, p.part_rows * D)) p.o_part[base + h * stride + d] = val;
+      else if (DA_IN(p, base + h * stride + d, p.part_rows * D))
+        st_keep(p.o_part + base + h * stride + d, val, keep);
     }
   }
 }

@@ -698,12 +698,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const size_t stride = single ? size_t(D) : size_t(p.max_splits) * D;
       const size_t base = single ? (bh0 + hb) * D + t_row
                                  : ((bh0 + hb) * p.max_splits + it.split) * D + t_row;
+      const uint64_t keep = l2_policy_evict_last();  // partials: read back by the combine
 #pragma unroll
       for (int h = 0; h < HT; ++h)
         if (hb + h < nheads) {
           if (single) store_out(p, base + h * stride, o[h] * inv_l[h]);
           else if (DA_IN(p, base + h * stride, p.part_rows * D))
-            p.o_part[base + h * stride] = o[h] * inv_l[h];
+            st_keep(p.o_part + base + h * stride, o[h] * inv_l[h], keep);
         }
       if ((!single || p.lse_out) && quarter == 0 && lane < HT && hb + lane < nheads) {
         float m_h = m_run[0], l_h = L[0];
@@ -716,7 +717,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const float lse2 = l_h > 0.f ? m_h + log2f(l_h) : -INFINITY;
         if (!single) {
           if (DA_IN(p, (bh0 + hb + lane) * p.max_splits + it.split, p.part_rows))
-            p.lse_part[(bh0 + hb + lane) * p.max_splits + it.split] = lse2;
+            st_keep(p.lse_part + (bh0 + hb + lane) * p.max_splits + it.split, lse2,
+                    l2_policy_evict_last());
         } else if (DA_IN(p, bh0 + hb + lane, size_t(p.B) * p.h_q)) {
           p.lse_out[bh0 + hb + lane] = lse2 * kLn2;
         }

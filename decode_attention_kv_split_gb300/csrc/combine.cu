@@ -81,10 +81,6 @@ __device__ __forceinline__ int splits_of_head(const SplitParams& p, int bh, int 
   return nv;
 }
 
-template <int D>
-__device__ __forceinline__ int combine_splits(const SplitParams& p, int bh, int heads_per_cta) {
-  return splits_of_head<D>(p, bh, __ldg(p.seq_lens + bh / p.h_q), heads_per_cta);
-}
 
 // Merge of one query head's nv > 1 partials by the whole CTA.  Warp w takes
 // splits w, w + kWarps, ... in passes of NB splits in flight (vector loads
@@ -174,12 +170,15 @@ __global__ void __launch_bounds__(W * 32, 32 / W)
   // The next kernel on the stream may launch now: a split kernel's CTAs
   // cannot share an SM with a combine CTA (registers), so they take the SMs
   // this grid leaves free and wait there (griddepcontrol.wait) until it has
-  // completed, with their set-up done and no launch latency left.
+  // completed, with their set-up done and no launch latency left.  The
+  // sequence's length is read before the wait: the split grid read the same
+  // final value before it let this grid launch.
+  const int bh = blockIdx.x;
+  const int seq_len = __ldg(p.seq_lens + bh / p.h_q);
   allow_dependent_launch();
   wait_for_prerequisite_grid();
 
-  const int bh = blockIdx.x;
-  const int nv = combine_splits<D>(p, bh, heads_per_cta);
+  const int nv = splits_of_head<D>(p, bh, seq_len, heads_per_cta);
   if (nv <= 1) return;  // written by the split kernel, or out of range (CTA-uniform)
   // NB splits per warp in flight at once: one pass covers NB * kWarps
   // splits, 272 for d <= 128 (256 splits and the one that rows appended past

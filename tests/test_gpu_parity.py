@@ -121,6 +121,51 @@ def test_all_sequences_empty(o):
         assert torch.all(out == 0)
 
 
+@pytest.mark.parametrize("dtype,h_q", [(torch.float32, 8), (torch.bfloat16, 8), (torch.bfloat16, 64)],
+                         ids=["fp32_g4", "bf16_g4", "bf16_g32"])
+def test_all_sequences_empty_every_family(o, dtype, h_q):
+    """No rows anywhere, in every list mode (balanced pieces count an empty
+    sequence as one row so that its zero output is still written): every
+    output is exactly zero and no error bit is set."""
+    q, K, V, lens_t, _ = make_case(3, h_q, 2, 128, 64, [0, 0, 0], dtype)
+    for splits in (0, 1, 4, -1):
+        err = torch.zeros((), dtype=torch.int32, device="cuda")
+        out = gpu_decode(q, K, V, lens_t, num_splits=splits, dev_error=err)
+        assert torch.all(out == 0)
+        assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("dtype,h_q,h_kv", [(torch.float32, 8, 2), (torch.bfloat16, 8, 2),
+                                            (torch.bfloat16, 32, 1)],
+                         ids=["fp32_g4", "bf16_g4", "bf16_g32"])
+def test_zero_scale_is_the_mean_of_v(o, dtype, h_q, h_kv):
+    """scale = 0 makes every score 0, so every weight is 1/n and each query
+    head's output is the plain mean of its KV head's first n rows of V:
+    checked against the oracle and against that mean taken directly."""
+    lens = [300, 129, 1]
+    q, K, V, lens_t, _ = make_case(3, h_q, h_kv, 128, 300, lens, dtype, seed=11)
+    g = h_q // h_kv
+    for splits in (0, 3, -1):
+        out = gpu_decode(q, K, V, lens_t, num_splits=splits, scale=0.0)
+        check_against_oracle(o, q, K, V, lens_t, 0.0, out, TOL[dtype])
+        for b, n in enumerate(lens):
+            mean = V[b, :, :n].double().mean(dim=1)        # [h_kv, d_v]
+            want = mean.repeat_interleave(g, dim=0)         # query head h reads kv head h // g
+            assert torch.max(torch.abs(out[b].double() - want)).item() <= TOL[dtype]
+
+
+def test_large_n_max_few_rows(o):
+    """A cache sized for 262144 rows that holds a few hundred: the host plans
+    for n_max, the device splits the actual lengths.  Only the rows below the
+    lengths reach the oracle (the rest are NaN and must never be read)."""
+    B, h_q, h_kv, d, n_max = 2, 16, 2, 64, 1 << 18
+    q, K, V, lens_t, scale = make_case(B, h_q, h_kv, d, n_max, [5, 200], torch.bfloat16, seed=5)
+    for splits in (0, 2, 300, -1):
+        out = gpu_decode(q, K, V, lens_t, num_splits=splits)
+        check_against_oracle(o, q, K[:, :, :256], V[:, :, :256], lens_t, scale, out,
+                             TOL[torch.bfloat16])
+
+
 def test_out_of_range_lengths_are_clamped_and_flagged(o):
     q, K, V, _, scale = make_case(2, 4, 2, 64, 100, [100, 50], torch.float32)
     err = torch.zeros((), dtype=torch.int32, device="cuda")

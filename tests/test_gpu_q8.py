@@ -125,6 +125,73 @@ def test_q8_decode_matches_oracle(o, kind, case, splits):
     _check(out, want, TOL)
 
 
+def _gpu_q8_checked(kind, q, kc, ks, vc, vs, lens, num_splits=0, scale=None):
+    """decode_attn_q8 with an explicit scale and the device error word: (out, error bits)."""
+    dev = torch.device("cuda")
+    tdt = KINDS[kind][1]
+    err = torch.zeros((), dtype=torch.int32, device=dev)
+    out = api.decode_attn_q8(q.to(dev), _codes_tensor(kc, tdt).to(dev), _codes_tensor(vc, tdt).to(dev),
+                             torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev), lens.to(dev),
+                             scale=scale, num_splits=num_splits, dev_error=err)
+    torch.cuda.synchronize()
+    return out.cpu(), int(err.item())
+
+
+@pytest.mark.parametrize("kind", list(KINDS))
+def test_q8_all_sequences_empty(o, kind):
+    """No rows anywhere (every cached row NaN-coded), chunked and balanced
+    lists: every output is exactly zero and no error bit is set."""
+    k = KINDS[kind][0]
+    for d in (64, 128):
+        _, q, kc, ks, vc, vs, lens_t = make_q8_case(o, k, 3, 8, 2, d, 64, [0, 0, 0], seed=d)
+        for splits in (0, 1, 4, -1):
+            out, err = _gpu_q8_checked(kind, q, kc, ks, vc, vs, lens_t, splits)
+            assert torch.all(out == 0)
+            assert err == 0
+
+
+@pytest.mark.parametrize("kind", list(KINDS))
+def test_q8_zero_rows(o, kind):
+    """Cached rows that are entirely zero quantize to zero codes with scale 0
+    (the format's degenerate row): a zero K row scores 0, a zero V row adds
+    weight and no value."""
+    k = KINDS[kind][0]
+    B, h_q, h_kv, d, n_max, lens = 2, 8, 2, 128, 300, [300, 130]
+    w = W.custom(B=B, h_q=h_q, h_kv=h_kv, d_k=d, n=max(lens), n_max=n_max, dtype=torch.float32)
+    K, V = W.cache(w, 7)
+    K[:, :, ::3] = 0.0
+    V[:, :, 1::4] = 0.0
+    kc, ks = o.quantize(K.numpy(), k)
+    vc, vs = o.quantize(V.numpy(), k)
+    assert np.all(ks[:, :, ::3] == 0) and np.all(vs[:, :, 1::4] == 0)
+    for b in range(B):  # unused rows: NaN codes and scales, as in make_q8_case
+        kc[b, :, lens[b]:] = 0x7F
+        vc[b, :, lens[b]:] = 0x7F
+        ks[b, :, lens[b]:] = np.nan
+        vs[b, :, lens[b]:] = np.nan
+    q = W.query(w, 7).to(torch.bfloat16)
+    lens_t = torch.tensor(lens, dtype=torch.int32)
+    want = oracle_decode_q8(o, k, q, kc, ks, vc, vs, lens_t, w.scale)
+    for splits in (0, 3, -1):
+        out, err = _gpu_q8_checked(kind, q, kc, ks, vc, vs, lens_t, splits)
+        assert err == 0
+        _check(out, want, TOL)
+
+
+@pytest.mark.parametrize("kind", list(KINDS))
+def test_q8_peaked_softmax(o, kind):
+    """Large scores concentrate the weight on few rows (stresses the score
+    arithmetic and the fp16 head + remainder of P): scale 0.5 and 1.0 instead
+    of 1/sqrt(128)."""
+    k = KINDS[kind][0]
+    _, q, kc, ks, vc, vs, lens_t = make_q8_case(o, k, 2, 8, 2, 128, 400, [400, 37], seed=3)
+    for scale in (0.5, 1.0):
+        want = oracle_decode_q8(o, k, q, kc, ks, vc, vs, lens_t, scale)
+        out, err = _gpu_q8_checked(kind, q, kc, ks, vc, vs, lens_t, 4, scale=scale)
+        assert err == 0
+        _check(out, want, TOL)
+
+
 @pytest.mark.parametrize("kind", list(KINDS))
 def test_q8_tile_boundaries(o, kind):
     lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257]
